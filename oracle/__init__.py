@@ -1,0 +1,185 @@
+"""fp64 CPU oracle for the spatial self-attention block (TEST INFRASTRUCTURE).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never imports it, and
+it imports nothing from the CUDA library: the two share no code.
+
+The arithmetic lives in ``ssa_oracle.c`` (plain loops, fp64, OpenMP over
+independent rows); this module only marshals numpy arrays through ``ctypes``.
+What the block computes is stated on the tensortonic page
+"diffusion-l03-spatial-self-attention" (problem statement and block equation):
+
+    out = x + image([O_1..O_n] Wo^T + bo),  O_j = softmax(Q_j K_j^T / sqrt(d)) V_j,
+    Q/K/V = tokens(GN(x)) W^T + b,  GN: G groups, eps 1e-5, affine.
+
+Parity is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``
+(library special cases, closed forms, invariants, brute force and the pages'
+worked examples).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libssa_oracle.so")
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def build(verbose: bool = False) -> str:
+    """Compile ssa_oracle.c into oracle/libssa_oracle.so (gcc, -O2, OpenMP).
+
+    No -ffast-math: every fp64 operation keeps IEEE semantics.  Falls back to a
+    single-threaded build when the compiler has no OpenMP runtime.
+    """
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", _LIB_PATH, _SRC, "-lm"]
+    for extra in (["-fopenmp"], []):
+        cmd = base[:3] + extra + base[3:]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode == 0:
+            if verbose:
+                print(" ".join(cmd))
+            return _LIB_PATH
+    raise RuntimeError("oracle build failed:\n" + r.stderr)
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.ssa_oracle_gn_stats.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp]
+    lib.ssa_oracle_gn_stats.restype = ctypes.c_int
+    lib.ssa_oracle_forward.argtypes = (
+        [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ip, ctypes.c_int] + [dp] * 9
+    )
+    lib.ssa_oracle_forward.restype = ctypes.c_int
+    lib.ssa_oracle_round.argtypes = [dp, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]
+    lib.ssa_oracle_round.restype = None
+    lib.ssa_oracle_num_threads.argtypes = []
+    lib.ssa_oracle_num_threads.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _dptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    """Exact up-conversion of stored values (numpy or torch CPU) to fp64."""
+    if hasattr(a, "detach"):  # a torch tensor: fp32 and bf16 widen exactly
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+PARAM_KEYS = ("norm_weight", "norm_bias", "q_weight", "q_bias", "k_weight", "k_bias",
+              "v_weight", "v_bias", "out_weight", "out_bias")
+
+
+def num_threads() -> int:
+    return int(_load().ssa_oracle_num_threads())
+
+
+def gn_stats(x, num_groups: int):
+    """Per (sample, group) mean and 1/sqrt(var + 1e-5), two-pass fp64."""
+    x = _f64(x)
+    B, C = x.shape[0], x.shape[1]
+    N = int(np.prod(x.shape[2:]))
+    mean = np.empty((B, num_groups))
+    rstd = np.empty((B, num_groups))
+    rc = _load().ssa_oracle_gn_stats(_dptr(x), B, C, N, num_groups, _dptr(mean), _dptr(rstd))
+    if rc != 0:
+        raise ValueError("bad shape for group norm")
+    return mean, rstd
+
+
+def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()):
+    """Run the block in fp64.
+
+    x: (B, C, H, W); params: the 10 tensors keyed as on the page.
+    qidx: None (every pixel) or a 1-D array of pixel indices (row i*W + j)
+    shared by every sample.  Returns a dict with 'y' (B, C, nq) = the branch
+    image([O] Wo^T + bo) at those pixels, and any of 'mean', 'rstd', 'z', 'q',
+    'k', 'v', 'o', 'p' named in ``want``.
+    """
+    x = _f64(x)
+    B, C, H, W = x.shape
+    N = H * W
+    p = {k: _f64(params[k]) for k in PARAM_KEYS}
+    G, nh = num_groups, num_heads
+    if qidx is not None:
+        qi = np.ascontiguousarray(np.asarray(qidx, dtype=np.int32))
+        nq = int(qi.size)
+        qptr = qi.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+    else:
+        qi, nq, qptr = None, N, None
+    out = {"y": np.empty((B, C, nq))}
+    shapes = {"mean": (B, G), "rstd": (B, G), "z": (B, N, C), "q": (B, nq, C),
+              "k": (B, N, C), "v": (B, N, C), "o": (B, nq, C), "p": (B, nh, nq, N)}
+    for k in want:
+        out[k] = np.empty(shapes[k])
+    rc = _load().ssa_oracle_forward(
+        _dptr(x), B, C, H, W, G, nh,
+        *[_dptr(p[k]) for k in PARAM_KEYS],
+        qptr, nq,
+        _dptr(out["y"]), *[_dptr(out.get(k)) for k in ("mean", "rstd", "z", "q", "k", "v", "o", "p")])
+    if rc != 0:
+        raise ValueError(f"oracle rejected the problem (rc={rc})")
+    return out
+
+
+def round_to(v: np.ndarray, dtype: str) -> np.ndarray:
+    """Round fp64 values once, to nearest-even, to 'f32' (float32 array) or
+    'bf16' (uint16 array of bf16 bit patterns)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    if dtype == "f32":
+        out = np.empty(v.shape, dtype=np.float32)
+        code = F32
+    elif dtype == "bf16":
+        out = np.empty(v.shape, dtype=np.uint16)
+        code = BF16
+    else:
+        raise ValueError(dtype)
+    _load().ssa_oracle_round(_dptr(v), v.size, code, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to fp64 exactly."""
+    u32 = np.asarray(bits, dtype=np.uint32) << 16
+    return u32.view(np.float32).astype(np.float64)
+
+
+def block(x, params: dict, num_groups: int, num_heads: int, qidx=None):
+    """The full block with the page's dtype rule: returns (out_f64, y_f64)
+    where out_f64 is x + y rounded once to x's dtype and widened back to fp64
+    for comparison.  x's dtype is read from a torch tensor ('bf16' when
+    torch.bfloat16) or taken as fp32 for anything else."""
+    dt = "bf16" if (hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16") else "f32"
+    xf = _f64(x)
+    r = forward(xf, params, num_groups, num_heads, qidx=qidx)
+    y = r["y"]
+    B, C = xf.shape[:2]
+    xs = xf.reshape(B, C, -1)
+    if qidx is not None:
+        xs = xs[:, :, np.asarray(qidx)]
+    exact = xs + y
+    rounded = round_to(exact, dt)
+    if dt == "bf16":
+        out = bf16_bits_to_f64(rounded)
+    else:
+        out = rounded.astype(np.float64)
+    return out, y
