@@ -1,0 +1,398 @@
+// attention.cu -- O_j = softmax(Q_j K_j^T / sqrt(d)) V_j per (sample, head)
+// (tensortonic "diffusion-l03-spatial-self-attention", block equation; the
+// softmax runs over the key axis and the head outputs are concatenated along
+// channels in head order; worked example 1 divides the scores by sqrt(2) for
+// d = 2).
+//
+// Flash-style: one CTA owns 128 queries of one (sample, head) -- and one of
+// the two 256-column halves of O when the padded head dim exceeds 256 -- and
+// walks the keys in tiles of 128, so the N x N score matrix never exists.
+//   warp 0     TMA producer: Q once, then K tiles and V^T tiles through a
+//              ring of 32 KB stages (128-byte swizzled K-major boxes)
+//   warp 1     tcgen05 MMA issuer: S = Q K^T into one of two tensor-memory
+//              score buffers, O += P V into a tensor-memory accumulator
+//   warps 2-5  softmax: one query row per thread.  Scores are read from
+//              tensor memory, the 1/sqrt(d) scale and log2(e) fold into one
+//              FFMA ahead of ex2, P is rounded to fp16 into a swizzled shared
+//              tile for the next MMA.  The running maximum is only raised
+//              (and O rescaled in tensor memory) when it grows by more than
+//              2^8, which keeps every P <= 256 and is exact after the final
+//              division by the row sum.
+// Keys past N in the last tile are zero-filled by TMA and masked to -inf.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ssa {
+namespace {
+
+constexpr int BQ = 128;
+constexpr int BKV = 128;
+constexpr int STAGE = 32768;
+constexpr int THREADS = 192;
+constexpr int MAX_SMEM = 232448;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+struct AttnArgs {
+  int N, h, d, dp, ldc, d_o, n_oc, nqb, nkc, nvc, nst, ntiles;
+  float sl2;  // log2(e) / sqrt(d)
+  uint16_t *o;
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+
+struct Layout {
+  uint32_t q, p, ring, bars;
+};
+__host__ __device__ inline Layout layout(int nqb, int nst) {
+  Layout L;
+  L.q = 0;
+  L.p = nqb * 16384;
+  L.ring = L.p + 32768;
+  L.bars = L.ring + nst * STAGE;
+  return L;
+}
+__host__ __device__ inline int nbars(int nst) { return 2 * nst + 6; }
+__host__ __device__ inline uint32_t smem_bytes(int nqb, int nst) {
+  return layout(nqb, nst).bars + nbars(nst) * 8 + 16 + 1024;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int nst = args.nst;
+  const Layout L = layout(args.nqb, nst);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + nst;
+  uint64_t *q_full = bars + 2 * nst;
+  uint64_t *s_full = q_full + 1;  // [2]
+  uint64_t *p_full = s_full + 2;
+  uint64_t *o_done = p_full + 1;
+  uint64_t *drain = o_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nbars(nst));
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x / args.n_oc;
+  const int oc = blockIdx.x % args.n_oc;
+  const int bh = blockIdx.y;
+  const int q0 = qt * BQ;
+  const int n = args.ntiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, args.err, args.timeout_ns};
+  const uint32_t TM_O = 256;  // O accumulator columns [256, 256 + d_o)
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, (uint32_t)(args.nqb * 16384));
+      for (int qb = 0; qb < args.nqb; ++qb) tma_load_3d(sm + L.q + qb * 16384, &qmap, q_full, qb * 64, q0, bh);
+      auto acquire = [&](int i) -> bool {
+        return i < nst || mbar_wait(&empty[i % nst], ((i / nst) - 1) & 1, ab);
+      };
+      auto load_k = [&](int j) {
+        for (int kc = 0; kc < args.nkc && ok; ++kc) {
+          if (!acquire(it)) { ok = false; break; }
+          const int s = it % nst;
+          const int nblk = min(2, args.nqb - 2 * kc);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(nblk * 16384));
+          for (int bl = 0; bl < nblk; ++bl)
+            tma_load_3d(sm + L.ring + s * STAGE + bl * 16384, &kmap, &full[s], (2 * kc + bl) * 64, j * BKV, bh);
+          ++it;
+        }
+      };
+      auto load_v = [&](int j) {
+        for (int vc = 0; vc < args.nvc && ok; ++vc) {
+          if (!acquire(it)) { ok = false; break; }
+          const int s = it % nst;
+          uint8_t *dst = sm + L.ring + s * STAGE;
+          if (args.nvc == 1) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * args.d_o * 128));
+            tma_load_3d(dst, &vmap, &full[s], j * BKV, oc * args.d_o, bh);
+            tma_load_3d(dst + args.d_o * 128, &vmap, &full[s], j * BKV + 64, oc * args.d_o, bh);
+          } else {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(args.d_o * 128));
+            tma_load_3d(dst, &vmap, &full[s], j * BKV + 64 * vc, oc * args.d_o, bh);
+          }
+          ++it;
+        }
+      };
+      load_k(0);
+      if (n > 1) load_k(1);
+      for (int j = 0; j < n && ok; ++j) {
+        load_v(j);
+        if (j + 2 < n) load_k(j + 2);
+      }
+      // Never leave with a copy in flight.
+      mbar_wait_drain(q_full, 0, ab.limit_ns);
+      for (int i = (it > nst ? it - nst : 0); i < it; ++i)
+        mbar_wait_drain(&full[i % nst], (i / nst) & 1, ab.limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_f16(BQ, BKV);
+      const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.d_o);
+      const uint32_t q_addr = smem_u32(sm + L.q);
+      const uint32_t p_addr = smem_u32(sm + L.p);
+      const uint32_t ring = smem_u32(sm + L.ring);
+      const int ksteps = args.dp / 16;
+      int it = 0;
+      bool ok = true, issued = false;
+      auto issue_s = [&](int buf) {
+        for (int kc = 0; kc < args.nkc && ok; ++kc) {
+          const int s = it % nst;
+          if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const int nblk = min(2, args.nqb - 2 * kc);
+          for (int bl = 0; bl < nblk; ++bl) {
+            const int qb = 2 * kc + bl;
+            for (int kk = 0; kk < 4; ++kk) {
+              const int ks = qb * 4 + kk;
+              if (ks >= ksteps) break;
+              mma_f16_ss(tmem + (uint32_t)(buf * BKV), sdesc_k128(q_addr + qb * 16384 + kk * 32),
+                         sdesc_k128(ring + s * STAGE + bl * 16384 + kk * 32), idesc_s, ks > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&empty[s]);
+          issued = true;
+          ++it;
+        }
+        if (ok) mma_commit(&s_full[buf]);
+      };
+      auto issue_pv = [&](int j) {
+        for (int vc = 0; vc < args.nvc && ok; ++vc) {
+          const int s = it % nst;
+          if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const int h0 = args.nvc == 1 ? 0 : vc;
+          const int h1 = args.nvc == 1 ? 2 : vc + 1;
+          for (int vh = h0; vh < h1; ++vh) {
+            const uint32_t vaddr = ring + s * STAGE + (args.nvc == 1 ? vh * args.d_o * 128 : 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(tmem + TM_O, sdesc_k128(p_addr + vh * 16384 + kk * 32), sdesc_k128(vaddr + kk * 32),
+                         idesc_o, (j > 0 || vh > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          issued = true;
+          ++it;
+        }
+        if (ok) mma_commit(o_done);
+      };
+      if (!mbar_wait(q_full, 0, ab)) ok = false;
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (n > 1) issue_s(1);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        if (!mbar_wait(p_full, j & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(j);
+        if (j + 2 < n) issue_s(j & 1);
+      }
+      if (!ok && issued) {
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0, ab.limit_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int query = q0 + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t p_tile = smem_u32(sm + L.p);
+    const float sl2 = args.sl2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int buf = j & 1;
+      if (!mbar_wait(&s_full[buf], (j >> 1) & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + (uint32_t)(buf * BKV + 32 * c), r[c]);
+      tmem_wait_ld();
+      const int kvalid = min(BKV, args.N - j * BKV);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (32 * c + i < kvalid) mx = fmaxf(mx, __uint_as_float(r[c][i]));
+      const float m_new = fmaxf(m_used, mx * sl2);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + RESCALE_LOG2) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+        rescale = true;
+      }
+      const float neg_m = -m_used;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int kidx = 32 * c + i;
+          const float e0 = kidx < kvalid ? ex2_approx(fmaf(__uint_as_float(r[c][i]), sl2, neg_m)) : 0.f;
+          const float e1 = kidx + 1 < kvalid ? ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), sl2, neg_m)) : 0.f;
+          sum += e0 + e1;
+          pk[(32 * c + i) >> 1] = pack_half2(e0, e1);
+        }
+      l = l * alpha + sum;
+      if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, ab)) { ok = false; break; }
+      if (rescale) {
+        tc_fence_after();
+        for (int cc = 0; cc < args.d_o / 16; ++cc) {
+          uint32_t t[16];
+          tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+          tmem_st16(lane_base + TM_O + (uint32_t)(cc * 16), t);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_shared_v4(p_tile + (c >> 3) * 16384 + sw128_offset((uint32_t)row, (uint32_t)(c & 7)), pk[4 * c],
+                     pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && mbar_wait(o_done, (n - 1) & 1, ab)) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      const int b = bh / args.h, hd = bh % args.h;
+      const bool vec = (args.d % 8) == 0;
+      uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
+      for (int cc = 0; cc < args.d_o / 16; ++cc) {
+        uint32_t t[16];
+        tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
+        tmem_wait_ld();
+        if (query >= args.N) continue;
+        const int e0 = oc * args.d_o + cc * 16;
+        if (vec && e0 + 16 <= args.d) {
+          uint4 w0, w1;
+          w0.x = pack_half2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
+          w0.y = pack_half2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
+          w0.z = pack_half2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
+          w0.w = pack_half2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
+          w1.x = pack_half2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
+          w1.y = pack_half2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
+          w1.z = pack_half2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
+          w1.w = pack_half2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
+          reinterpret_cast<uint4 *>(orow + e0)[0] = w0;
+          reinterpret_cast<uint4 *>(orow + e0)[1] = w1;
+        } else {
+          for (int i = 0; i < 16; ++i) {
+            if (e0 + i < args.d) {
+              const __half hv = __float2half_rn(__uint_as_float(t[i]) * inv);
+              orow[e0 + i] = *reinterpret_cast<const uint16_t *>(&hv);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
+                     const KParams &kp, cudaStream_t st) {
+  CUtensorMap qmap, kmap, vmap;
+  const uint64_t BH = (uint64_t)dm.B * dm.h;
+  {
+    const uint64_t dims[3] = {(uint64_t)dm.ldq, (uint64_t)dm.N, BH};
+    const uint64_t strides[2] = {(uint64_t)dm.ldq * 2, (uint64_t)dm.N * dm.ldq * 2};
+    const uint32_t box[3] = {64, BQ, 1};
+    if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+    if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, BH};
+    const uint64_t strides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
+    const uint32_t box[3] = {64, (uint32_t)dm.d_o, 1};
+    if (encode_tiled(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+  }
+  AttnArgs a{};
+  a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
+  a.nqb = (dm.dp + 63) / 64;
+  a.nkc = (a.nqb + 1) / 2;
+  a.nvc = dm.d_o <= 128 ? 1 : 2;
+  a.ntiles = (dm.N + BKV - 1) / BKV;
+  int max_smem = MAX_SMEM, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int nst = (int)(((long long)max_smem - (long long)smem_bytes(a.nqb, 0)) / (STAGE + 16));
+  if (nst > 6) nst = 6;
+  if (nst < 2) return 2;
+  a.nst = nst;
+  a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
+  a.o = o;
+  a.err = kp.err;
+  a.timeout_ns = kp.timeout_ns;
+  const uint32_t smem = smem_bytes(a.nqb, nst);
+  cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const dim3 grid((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
+  attention_kernel<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+}  // namespace ssa

@@ -1,0 +1,78 @@
+// internal.h -- host-side declarations shared by the launcher and the kernel
+// translation units: derived sizes/layouts and the per-kernel launch wrappers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ssa {
+
+// Sizes and internal layouts derived from one problem.
+//   dp  : head dim padded to the MMA K granularity (16; 32 above 256 so that
+//         the two output halves each stay a multiple of 16)
+//   ldq : row pitch (elements) of Q and K, a whole number of 64-element
+//         swizzle rows
+//   ldn : row pitch of V^T (pixels), 16-byte aligned
+//   ldc : row pitch of packed weights and O (channels), 16-byte aligned
+//   n_oc, d_o : the attention output of one head is produced in n_oc slices
+//         of d_o columns (one slice per CTA); n_oc = 2 when dp > 256
+struct Dims {
+  int B, C, H, W, N, G, h, d, dp, ldq, ldn, ldc, n_oc, d_o, ntot;
+};
+
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+inline Dims make_dims(int B, int C, int H, int W, int G, int h) {
+  Dims s{};
+  s.B = B; s.C = C; s.H = H; s.W = W; s.N = H * W; s.G = G; s.h = h;
+  s.d = (h > 0) ? C / h : 0;
+  s.dp = (s.d > 256) ? round_up(s.d, 32) : round_up(s.d, 16);
+  s.ldq = round_up(s.dp, 64);
+  s.ldn = round_up(s.N, 8);
+  s.ldc = round_up(C, 8);
+  s.n_oc = (s.dp > 256) ? 2 : 1;
+  s.d_o = s.dp / s.n_oc;
+  s.ntot = 3 * h * s.dp;
+  return s;
+}
+
+// Arguments every pipelined kernel receives for its bounded waits.
+struct KParams {
+  uint32_t *err;        // device error word
+  uint64_t timeout_ns;  // limit of one spin wait
+};
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// dims/strides innermost first; strides in bytes for dims 1..rank-1.
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                      CUtensorMapSwizzle swz);
+
+// ---- launch wrappers (each returns the launch error, if any) ----
+cudaError_t launch_gn_stats(const void *x, int B, int C, int N, int G, int dtype, const void *gw,
+                            const void *gb, float *mean, float *rstd, float *a, float *s, int num_sms,
+                            cudaStream_t st);
+
+cudaError_t launch_pack_weights(const Dims &dm, int dtype, const void *wq, const void *bq, const void *wk,
+                                const void *bk, const void *wv, const void *bv, const void *wo,
+                                const void *bo, uint16_t *w_qkv, float *b_qkv, uint16_t *w_o, float *b_o,
+                                cudaStream_t st);
+
+// Copy x [B][C][N] into [B][C][ldx] with ldx*esize a multiple of 16 bytes.
+cudaError_t launch_pad_x(const void *x, int B, int C, int N, int ldx, int esize, void *dst, cudaStream_t st);
+
+// Returns 0 on success, 1 when a tensor map could not be encoded, 2 on a launch error.
+int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const float *ga, const float *gs,
+                    const uint16_t *w_qkv, const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt,
+                    const KParams &kp, cudaStream_t st);
+
+int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
+                     const KParams &kp, cudaStream_t st);
+
+int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t *w_o, const float *b_o,
+                    const void *x, void *out, const KParams &kp, cudaStream_t st);
+
+cudaError_t launch_timeout_probe(const KParams &kp, cudaStream_t st);
+
+}  // namespace ssa

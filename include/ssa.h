@@ -1,0 +1,175 @@
+/*
+ * ssa.h -- C ABI of the GB300 (sm_103a) spatial self-attention block.
+ *
+ * The block (tensortonic "diffusion-l03-spatial-self-attention", problem
+ * statement and block equation):
+ *
+ *   Z = tokens(GN(x));  Q = Z Wq^T + bq;  K = Z Wk^T + bk;  V = Z Wv^T + bv;
+ *   O_j = softmax(Q_j K_j^T / sqrt(d)) V_j;  out = x + image([O_1..O_n] Wo^T + bo)
+ *
+ * x is (B, C, H, W); GN has num_groups groups, eps 1e-5 and the affine
+ * norm_weight / norm_bias; pixel (i, j) is token row i*W + j; d = C/num_heads
+ * and head j owns channels [j*d, (j+1)*d).  The result has x's dtype.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated; the
+ *    library never frees them.  Tensors are dense and contiguous.
+ *  - x and out are NCHW.  Weights are (C_out, C_in) row-major, as a linear
+ *    layer stores them; the ten parameters share x's dtype.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on it: no host synchronisation, no
+ *    host<->device copy and no allocation happens inside ssa_forward*,
+ *    ssa_gn_stats, ssa_qkv_project, ssa_attention or ssa_out_project.
+ *  - Argument errors are returned at once and nothing is launched.  Errors
+ *    raised on the device (a bounded wait that expired) are latched in a
+ *    device flag and returned by ssa_get_device_status().
+ *  - The 16-bit tensor-core operand type is fp16 (fp32 accumulation, fp32
+ *    softmax statistics).
+ */
+#ifndef SSA_H
+#define SSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSA_F32 = 0,   /* IEEE binary32 */
+    SSA_BF16 = 1   /* bfloat16 */
+} ssa_dtype;
+
+typedef enum {
+    SSA_OK = 0,
+    SSA_ERR_CONSTRAINT = 1,  /* C % num_groups, C % num_heads, or a size <= 0
+                                (E_CONSTRAINT in the HNDL attention operator doc) */
+    SSA_ERR_DTYPE = 2,       /* dtype is not SSA_F32 / SSA_BF16 */
+    SSA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+    SSA_ERR_UNSUPPORTED = 4, /* head dim above 512, or a size beyond the grid limits */
+    SSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than ssa_*workspace_size */
+    SSA_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed (see ssa_last_error_string) */
+    SSA_ERR_TIMEOUT = 7,     /* a bounded device-side wait expired (device flag) */
+    SSA_ERR_NULL = 8         /* a required pointer is NULL */
+} ssa_status;
+
+typedef struct ssa_plan ssa_plan;
+
+/* ---------------------------------------------------------------- block --- */
+
+/* Bytes of device workspace ssa_forward needs for this problem (packed
+ * weights, GN scale/shift, Q, K, V^T and O).  0 on a bad shape. */
+size_t ssa_workspace_size(int B, int C, int H, int W, int num_groups, int num_heads,
+                          ssa_dtype dtype);
+
+/* One-shot forward of the whole block (the page's f(x, params, num_groups,
+ * num_heads)).  Packs the weights into `workspace` on every call, then runs
+ * GN statistics -> QKV projection (GN affine + NCHW->token transpose fused in
+ * its prologue) -> flash attention -> output projection (bias, residual and
+ * NCHW store fused in its epilogue).  `out` may equal `x` (in place);
+ * otherwise it must not overlap any input.  workspace: device memory of at
+ * least ssa_workspace_size(...) bytes, 256-byte aligned, contents ignored. */
+ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                       const void *norm_weight, const void *norm_bias,
+                       const void *q_weight, const void *q_bias,
+                       const void *k_weight, const void *k_bias,
+                       const void *v_weight, const void *v_bias,
+                       const void *out_weight, const void *out_bias,
+                       void *out, ssa_dtype dtype,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Steady state: the parameters are constants of a module.  ssa_plan_create
+ * packs them once into device memory that the plan owns (cudaMalloc here and
+ * only here; freed by ssa_plan_destroy) and enqueues the pack on `stream`. */
+ssa_status ssa_plan_create(ssa_plan **plan, int C, int num_groups, int num_heads, ssa_dtype dtype,
+                           const void *norm_weight, const void *norm_bias,
+                           const void *q_weight, const void *q_bias,
+                           const void *k_weight, const void *k_bias,
+                           const void *v_weight, const void *v_bias,
+                           const void *out_weight, const void *out_bias, void *stream);
+size_t ssa_plan_workspace_size(const ssa_plan *plan, int B, int H, int W);
+ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H, int W, void *out,
+                               void *workspace, size_t workspace_bytes, void *stream);
+void ssa_plan_destroy(ssa_plan *plan);
+
+/* ------------------------------------------------- steps of the hot path --- *
+ * Each step of the block as its own launch, with the library's internal
+ * layouts, for per-step checks and timing.  Let
+ *   N = H*W,  d = C/num_heads,
+ *   dp = d rounded up to 16 (to 32 when d > 256)   -- MMA-padded head dim,
+ *   ldq = dp rounded up to 64,  ldn = N rounded up to 8,  ldc = C rounded up to 8.
+ * Layouts (fp16 unless stated):
+ *   mean, rstd   [B][G] fp32           gn_scale, gn_shift [B][C] fp32
+ *   w_qkv        [3][h][dp][ldc]       rows q|k|v, head-major, zero rows past d
+ *   b_qkv        [3][h][dp] fp32       zero past d
+ *   w_o          [C][ldc]              b_o [C] fp32
+ *   q, k         [B][h][N][ldq]        columns >= dp unspecified
+ *   vt           [B][h][dp][ldn]       V transposed per head; columns >= N unspecified
+ *   o            [B][N][ldc]           heads concatenated along channels
+ */
+
+/* GroupNorm statistics (Welford within a thread, Chan merges across threads
+ * and across the CTAs of a cluster): per (b, g) mean and rstd =
+ * 1/sqrt(var_biased + 1e-5), then the folded per-(b, c) affine
+ * gn_scale = rstd * norm_weight[c], gn_shift = norm_bias[c] - mean * gn_scale,
+ * so that GN(x)[b, c, :] = gn_scale[b, c] * x[b, c, :] + gn_shift[b, c].
+ * mean/rstd may be NULL. */
+ssa_status ssa_gn_stats(const void *x, int B, int C, int N, int num_groups, ssa_dtype dtype,
+                        const void *norm_weight, const void *norm_bias,
+                        float *mean, float *rstd, float *gn_scale, float *gn_shift, void *stream);
+
+/* Cast and pack the projection weights into the layouts above. */
+ssa_status ssa_pack_weights(int C, int num_heads, ssa_dtype dtype,
+                            const void *q_weight, const void *q_bias,
+                            const void *k_weight, const void *k_bias,
+                            const void *v_weight, const void *v_bias,
+                            const void *out_weight, const void *out_bias,
+                            uint16_t *w_qkv, float *b_qkv, uint16_t *w_o, float *b_o, void *stream);
+
+/* Q, K, V^T = tokens(gn_scale * x + gn_shift) w_qkv^T + b_qkv, written in the
+ * q / k / vt layouts (tcgen05 GEMM, M = pixels, N = 3*h*dp, K = C). */
+ssa_status ssa_qkv_project(const void *x, int B, int C, int H, int W, int num_heads, ssa_dtype dtype,
+                           const float *gn_scale, const float *gn_shift,
+                           const uint16_t *w_qkv, const float *b_qkv,
+                           uint16_t *q, uint16_t *k, uint16_t *vt, void *stream);
+
+/* O_j = softmax(Q_j K_j^T / sqrt(d)) V_j for every (b, head), never forming
+ * the N x N matrix; o receives the heads side by side (layout above). */
+ssa_status ssa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *vt,
+                         int B, int C, int N, int num_heads, uint16_t *o, void *stream);
+
+/* out = x + image(o w_o^T + b_o), rounded once to x's dtype (tcgen05 GEMM,
+ * M = pixels, N = C, K = C; bias, residual and the NCHW store in the
+ * epilogue).  out may equal x. */
+ssa_status ssa_out_project(const uint16_t *o, const uint16_t *w_o, const float *b_o,
+                           const void *x, int B, int C, int H, int W, ssa_dtype dtype,
+                           void *out, void *stream);
+
+/* --------------------------------------------------------- diagnostics --- */
+
+/* Synchronises `stream`, then reads and clears the device error flag:
+ * SSA_OK, SSA_ERR_TIMEOUT (a bounded wait expired; the kernel released its
+ * tensor memory and returned) or SSA_ERR_CUDA (a launch or execution error). */
+ssa_status ssa_get_device_status(void *stream);
+
+/* Limit of every device-side spin wait, in nanoseconds (default 2e9).
+ * Applies to launches made after the call. */
+void ssa_set_wait_timeout_ns(uint64_t ns);
+
+/* Launches one CTA whose mbarrier wait can never complete (nothing arrives),
+ * bounded by `timeout_ns`; the wait expires, latches SSA_ERR_TIMEOUT and the
+ * kernel returns.  Exercises the timeout path without faulting the GPU. */
+ssa_status ssa_debug_timeout_probe(uint64_t timeout_ns, void *stream);
+
+/* Human-readable detail of the last error returned on this thread. */
+const char *ssa_last_error_string(void);
+
+/* Number of kernel launches one ssa_forward / ssa_forward_planned call makes. */
+int ssa_launches_per_forward(int planned);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSA_H */

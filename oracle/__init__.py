@@ -64,6 +64,10 @@ def _load():
         [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ip, ctypes.c_int] + [dp] * 9
     )
     lib.ssa_oracle_forward.restype = ctypes.c_int
+    lib.ssa_oracle_attention.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [dp, dp]
+    lib.ssa_oracle_attention.restype = None
+    lib.ssa_oracle_out_proj.argtypes = [dp, dp, dp] + [ctypes.c_int] * 3 + [dp]
+    lib.ssa_oracle_out_proj.restype = None
     lib.ssa_oracle_round.argtypes = [dp, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]
     lib.ssa_oracle_round.restype = None
     lib.ssa_oracle_num_threads.argtypes = []
@@ -139,6 +143,29 @@ def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (rc={rc})")
     return out
+
+
+def attention(q, k, v, num_heads: int):
+    """The attention step alone, in fp64, from given Q (B, nq, C) and K, V
+    (B, N, C): per head softmax(Q_j K_j^T / sqrt(d)) V_j, heads side by side.
+    Returns O (B, nq, C)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, nq, C = q.shape
+    N = k.shape[1]
+    if C % num_heads:
+        raise ValueError("num_heads must divide C")
+    o = np.empty((B, nq, C))
+    _load().ssa_oracle_attention(_dptr(q), _dptr(k), _dptr(v), B, N, nq, C, num_heads, _dptr(o), None)
+    return o
+
+
+def out_proj(o, out_weight, out_bias):
+    """The output projection alone, in fp64: y (B, C, nq) = image(O Wo^T + bo)."""
+    o, w, b = _f64(o), _f64(out_weight), _f64(out_bias)
+    B, nq, C = o.shape
+    y = np.empty((B, C, nq))
+    _load().ssa_oracle_out_proj(_dptr(o), _dptr(w), _dptr(b), B, nq, C, _dptr(y))
+    return y
 
 
 def round_to(v: np.ndarray, dtype: str) -> np.ndarray:

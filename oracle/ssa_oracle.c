@@ -71,6 +71,72 @@ int ssa_oracle_gn_stats(const double *x, int B, int C, int N, int G,
     return 0;
 }
 
+/* ---- Step 3: attention from given Q, K, V --------------------------------
+ * q [B][nq][C] (the query rows), k, v [B][N][C], o [B][nq][C],
+ * p (optional) [B][h][nq][N].  Per head j: scores over all keys scaled by
+ * 1/sqrt(d), a softmax over the key axis (the maximum is subtracted only to
+ * keep exp() in range), then P V; head outputs side by side in head order. */
+void ssa_oracle_attention(const double *q, const double *k, const double *v, int B, int N, int nq, int C,
+                          int nh, double *o, double *p_out)
+{
+    const int d = C / nh;
+    const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * N);
+#pragma omp for collapse(2) schedule(static)
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < nq; ++t) {
+                const double *qr = q + ((long long)b * nq + t) * C;
+                double *orow = o + ((long long)b * nq + t) * C;
+                for (int j = 0; j < nh; ++j) {
+                    const int c0 = j * d;
+                    double smax = -INFINITY;
+                    for (int m = 0; m < N; ++m) {
+                        const double *kr = k + ((long long)b * N + m) * C;
+                        double acc = 0.0;
+                        for (int e = 0; e < d; ++e) acc += qr[c0 + e] * kr[c0 + e];
+                        s[m] = acc * scale;
+                        if (s[m] > smax) smax = s[m];
+                    }
+                    double den = 0.0;
+                    for (int m = 0; m < N; ++m) {
+                        s[m] = exp(s[m] - smax);
+                        den += s[m];
+                    }
+                    for (int m = 0; m < N; ++m) s[m] /= den;
+                    if (p_out) {
+                        double *pr = p_out + (((long long)b * nh + j) * nq + t) * N;
+                        for (int m = 0; m < N; ++m) pr[m] = s[m];
+                    }
+                    for (int e = 0; e < d; ++e) {
+                        double acc = 0.0;
+                        for (int m = 0; m < N; ++m)
+                            acc += s[m] * v[((long long)b * N + m) * C + c0 + e];
+                        orow[c0 + e] = acc;
+                    }
+                }
+            }
+        free(s);
+    }
+}
+
+/* ---- Step 4: output projection and image() --------------------------------
+ * o [B][nq][C] -> y [B][C][nq] = (o Wo^T + bo) with the pixel axis last. */
+void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, int B, int nq, int C, double *y)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < nq; ++t) {
+            const double *orow = o + ((long long)b * nq + t) * C;
+            for (int c = 0; c < C; ++c) {
+                double acc = 0.0;
+                for (int e = 0; e < C; ++e) acc += orow[e] * wo[(long long)c * C + e];
+                y[((long long)b * C + c) * nq + t] = acc + bo[c];
+            }
+        }
+}
+
 /* ---- The whole block ------------------------------------------------------
  * Inputs (all fp64, contiguous):
  *   x [B][C][H*W]; gw, gb, bq, bk, bv, bo [C]; wq, wk, wv, wo [C][C] (out, in).
@@ -102,8 +168,6 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
     if (!qidx) nq = N;
     if (nq <= 0) return -1;
     const int cg = C / G;
-    const int d = C / nh;
-    const double scale = 1.0 / sqrt((double)d);
 
     double *mean = (double *)malloc(sizeof(double) * B * G);
     double *rstd = (double *)malloc(sizeof(double) * B * G);
@@ -159,59 +223,9 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
             }
         }
 
-    /* 3. Per head j: scores over all keys scaled by 1/sqrt(d), a softmax over
-     *    the key axis (max subtracted for range only), then P V; the head
-     *    outputs are written back side by side in head order. */
-#pragma omp parallel
-    {
-        double *s = (double *)malloc(sizeof(double) * N);
-#pragma omp for collapse(2) schedule(static)
-        for (int b = 0; b < B; ++b)
-            for (int t = 0; t < nq; ++t) {
-                const double *qr = q + ((long long)b * nq + t) * C;
-                double *orow = o + ((long long)b * nq + t) * C;
-                for (int j = 0; j < nh; ++j) {
-                    const int c0 = j * d;
-                    double smax = -INFINITY;
-                    for (int m = 0; m < N; ++m) {
-                        const double *kr = k + ((long long)b * N + m) * C;
-                        double acc = 0.0;
-                        for (int e = 0; e < d; ++e) acc += qr[c0 + e] * kr[c0 + e];
-                        s[m] = acc * scale;
-                        if (s[m] > smax) smax = s[m];
-                    }
-                    double den = 0.0;
-                    for (int m = 0; m < N; ++m) {
-                        s[m] = exp(s[m] - smax);
-                        den += s[m];
-                    }
-                    for (int m = 0; m < N; ++m) s[m] /= den;
-                    if (p_out) {
-                        double *pr = p_out + (((long long)b * nh + j) * nq + t) * N;
-                        for (int m = 0; m < N; ++m) pr[m] = s[m];
-                    }
-                    for (int e = 0; e < d; ++e) {
-                        double acc = 0.0;
-                        for (int m = 0; m < N; ++m)
-                            acc += s[m] * v[((long long)b * N + m) * C + c0 + e];
-                        orow[c0 + e] = acc;
-                    }
-                }
-            }
-        free(s);
-    }
-
-    /* 4. Output projection, then image(): y[b][c][pixel]. */
-#pragma omp parallel for collapse(2) schedule(static)
-    for (int b = 0; b < B; ++b)
-        for (int t = 0; t < nq; ++t) {
-            const double *orow = o + ((long long)b * nq + t) * C;
-            for (int c = 0; c < C; ++c) {
-                double acc = 0.0;
-                for (int e = 0; e < C; ++e) acc += orow[e] * wo[(long long)c * C + e];
-                y[((long long)b * C + c) * nq + t] = acc + bo[c];
-            }
-        }
+    /* 3. Attention per head, then 4. the output projection and image(). */
+    ssa_oracle_attention(q, k, v, B, N, nq, C, nh, o, p_out);
+    ssa_oracle_out_proj(o, wo, bo, B, nq, C, y);
 
     if (mean_out) memcpy(mean_out, mean, sizeof(double) * B * G);
     if (rstd_out) memcpy(rstd_out, rstd, sizeof(double) * B * G);

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (block definition on the tensortonic page
+"diffusion-l03-spatial-self-attention"; the target accuracy of fp16 tensor-core
+operands with fp32 accumulation and fp32 softmax statistics):
+  * branch out - x:  relative L2 error <= 1e-2
+  * out:             max |delta| <= 5e-2
+Per-step checks use the oracle's steps on the GPU's own inputs to that step.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from diffusion_net_spatial_gb300 import workloads as wls
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 5e-2
+
+
+@pytest.fixture(scope="module")
+def ssa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_net_spatial_gb300 as m
+    m.load_library()
+    return m
+
+
+def _to_dev(x, p):
+    dev = torch.device("cuda:0")
+    return x.to(dev), {k: v.to(dev) for k, v in p.items()}
+
+
+def _compare(out_gpu, x, p, wl, qidx=None):
+    """Returns (rel_l2_branch, max_abs_out) against the oracle."""
+    ref, y = oracle.block(x, p, wl.num_groups, wl.num_heads, qidx=None if qidx is None else qidx.numpy())
+    B, C = x.shape[:2]
+    got = out_gpu.double().cpu().numpy().reshape(B, C, -1)
+    xs = x.double().numpy().reshape(B, C, -1)
+    if qidx is not None:
+        got = got[:, :, qidx.numpy()]
+        xs = xs[:, :, qidx.numpy()]
+    rel = np.linalg.norm((got - xs) - y) / max(np.linalg.norm(y), 1e-30)
+    mx = np.abs(got - ref).max()
+    return rel, mx
+
+
+def _run(ssa, wl, inplace=False):
+    x, p, qidx = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    if inplace:
+        out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads, out=xd)
+    else:
+        out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads)
+    st = ssa.ssa_get_device_status()
+    assert st == 0, ssa.ssa_last_error_string()
+    assert out.dtype == x.dtype and out.shape == x.shape
+    return _compare(out, x, p, wl, qidx)
+
+
+SMALL = [
+    # name, B, C, H, W, G, h, dtype
+    ("ragged-d64", 2, 128, 12, 20, 8, 2, "f32"),       # N = 240: one full 128 tile + ragged tail
+    ("ragged-d40", 1, 80, 9, 15, 8, 2, "f32"),         # d = 40 -> padded to 48; N = 135
+    ("ragged-d512", 1, 512, 10, 13, 32, 1, "f32"),     # d = 512: two 256-wide output halves; N = 130
+    ("d16-multihead", 2, 64, 5, 7, 4, 4, "f32"),       # N = 35 (not a multiple of 4: padded-x path)
+    ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
+    ("single-pixel", 3, 64, 1, 1, 64, 2, "f32"),       # H = W = 1, one channel per group
+    ("group1-head1", 1, 96, 6, 6, 1, 1, "f32"),        # one group, one head (d = 96)
+    ("d32-multitile", 1, 64, 16, 24, 8, 2, "f32"),     # N = 384: three key tiles
+    ("d128", 1, 256, 16, 16, 8, 2, "f32"),
+    ("d256", 1, 256, 12, 12, 8, 1, "f32"),
+    ("d320", 1, 320, 9, 9, 8, 1, "f32"),               # dp = 320 -> two 160-wide halves
+    ("ex1-shape", 1, 4, 2, 2, 2, 2, "f32"),            # worked example 1's shape (d = 2)
+    ("ex2-shape", 1, 2, 2, 3, 1, 1, "f32"),            # worked example 2's shape (H != W)
+    ("ex3-shape", 2, 4, 1, 1, 4, 2, "f32"),            # worked example 3's shape
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_block_small_shapes(ssa, case):
+    name, B, C, H, W, G, h, dt = case
+    wl = wls.custom(name, B, C, H, W, G, h, dt, seed=11)
+    rel, mx = _run(ssa, wl)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+@pytest.mark.parametrize("name", list(wls.WORKLOADS))
+def test_block_named_workloads(ssa, name):
+    """The five named shapes at full size; the largest is checked on its 512
+    seeded query pixels (every key), the others on every pixel."""
+    rel, mx = _run(ssa, wls.WORKLOADS[name])
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_in_place(ssa):
+    wl = wls.custom("inplace", 2, 128, 8, 16, 8, 2, "f32", seed=5)
+    rel, mx = _run(ssa, wl, inplace=True)
+    assert rel <= REL_L2 and mx <= MAX_ABS
+
+
+def test_planned_matches_one_shot_bitwise(ssa):
+    wl = wls.custom("plan", 2, 320, 16, 16, 32, 8, "f32", seed=6)
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    a = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads)
+    plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads)
+    b = plan.forward(xd)
+    c = plan.forward(xd)
+    assert ssa.ssa_get_device_status() == 0
+    assert torch.equal(a, b) and torch.equal(b, c)
+    plan.close()
+
+
+def test_gn_stats_step(ssa):
+    """GN statistics kernel against the oracle's two-pass fp64 statistics."""
+    for (B, C, H, W, G, dt, shift) in [(2, 320, 64, 64, 32, "f32", 0.0), (1, 512, 128, 128, 32, "f32", 3.0),
+                                        (8, 1280, 16, 16, 32, "bf16", 0.0), (3, 12, 5, 3, 4, "f32", -7.0)]:
+        wl = wls.custom("gn", B, C, H, W, G, 1, dt, seed=B + C, x_scale=2.0)
+        x, p, _ = wls.make_inputs(wl)
+        x = (x.float() + shift).to(x.dtype)
+        xd, pd = _to_dev(x, p)
+        mean, rstd, a, s = ssa.ssa_gn_stats(xd, G, pd["norm_weight"], pd["norm_bias"])
+        assert ssa.ssa_get_device_status() == 0
+        m_ref, r_ref = oracle.gn_stats(x, G)
+        np.testing.assert_allclose(mean.cpu().double().numpy(), m_ref, rtol=1e-5, atol=1e-5 * (1 + abs(shift)))
+        np.testing.assert_allclose(rstd.cpu().double().numpy(), r_ref, rtol=2e-5)
+        gw = p["norm_weight"].double().numpy()
+        gb = p["norm_bias"].double().numpy()
+        cg = C // G
+        a_ref = np.repeat(r_ref, cg, axis=1) * gw
+        s_ref = gb - np.repeat(m_ref, cg, axis=1) * a_ref
+        np.testing.assert_allclose(a.cpu().double().numpy(), a_ref, rtol=2e-5)
+        np.testing.assert_allclose(s.cpu().double().numpy(), s_ref, rtol=2e-5, atol=2e-5 * (1 + abs(shift)))
+
+
+def _step_inputs(ssa, wl):
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    _, _, a, s = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"])
+    packed = ssa.ssa_pack_weights(pd, wl.num_heads)
+    return x, p, xd, pd, a, s, packed
+
+
+STEP_SHAPES = [("d64", 2, 128, 12, 20, 8, 2, "f32"), ("d40", 1, 80, 16, 8, 8, 2, "f32"),
+               ("d512", 1, 512, 8, 32, 32, 1, "f32"), ("bf16", 2, 256, 8, 8, 16, 4, "bf16")]
+
+
+@pytest.mark.parametrize("case", STEP_SHAPES, ids=[c[0] for c in STEP_SHAPES])
+def test_qkv_attention_outproj_steps(ssa, case):
+    name, B, C, H, W, G, h, dt = case
+    wl = wls.custom(name, B, C, H, W, G, h, dt, seed=21)
+    x, p, xd, pd, a, s, pk = _step_inputs(ssa, wl)
+    N, d = H * W, C // h
+    q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], h)
+    assert ssa.ssa_get_device_status() == 0
+    r = oracle.forward(x, p, G, h, want=("q", "k", "v", "o"))
+    # Q/K/V against the oracle's projections
+    qg = q[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, N, C)
+    kg = k[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, N, C)
+    vg = vt[:, :, :d, :N].double().cpu().numpy().transpose(0, 3, 1, 2).reshape(B, N, C)
+    for got, ref in ((qg, r["q"]), (kg, r["k"]), (vg, r["v"])):
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 3e-3
+    # padded columns of Q and K are exactly zero
+    if d < q.shape[-1]:
+        dp = ssa.layout(B, C, H, W, h)["dp"]
+        assert torch.count_nonzero(q[..., d:dp]) == 0 and torch.count_nonzero(k[..., d:dp]) == 0
+    # attention on the GPU's own Q/K/V against the oracle's attention step
+    o = ssa.ssa_attention(q, k, vt, B, C, N, h)
+    assert ssa.ssa_get_device_status() == 0
+    o_ref = oracle.attention(qg, kg, vg, h)
+    og = o[..., :C].double().cpu().numpy()
+    assert np.linalg.norm(og - o_ref) / np.linalg.norm(o_ref) < 3e-3
+    assert np.abs(og - o_ref).max() < 2e-2
+    # out-projection on the GPU's own O against the oracle's projection step
+    out = ssa.ssa_out_project(o, pk["w_o"], pk["b_o"], xd)
+    assert ssa.ssa_get_device_status() == 0
+    y_ref = oracle.out_proj(og, p["out_weight"], p["out_bias"])
+    got = out.double().cpu().numpy().reshape(B, C, N) - x.double().numpy().reshape(B, C, N)
+    tol = 2e-2 if dt == "bf16" else 2e-3
+    assert np.linalg.norm(got - y_ref) / np.linalg.norm(y_ref) < tol
+
+
+def test_timeout_path_returns_status_and_context_survives(ssa):
+    """A wait that nothing ends expires after its limit, latches
+    SSA_ERR_TIMEOUT, and the context stays usable."""
+    ssa.ssa_debug_timeout_probe(2_000_000)   # 2 ms limit
+    assert ssa.ssa_get_device_status() == 7
+    assert ssa.ssa_get_device_status() == 0  # read-and-clear
+    rel, mx = _run(ssa, wls.WORKLOADS["tiny"])
+    assert rel <= REL_L2 and mx <= MAX_ABS
+
+
+def test_argument_errors(ssa):
+    wl = wls.WORKLOADS["tiny"]
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_forward(xd, pd, 7, 2)          # 7 does not divide 64
+    assert e.value.status == 1
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_forward(xd, pd, 8, 3)          # 3 does not divide 64
+    assert e.value.status == 1
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_forward(xd, pd, 8, 2, workspace=ws)
+    assert e.value.status == 5
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_forward(xd.double(), {k: v.double() for k, v in pd.items()}, 8, 2)
+    assert e.value.status == 2

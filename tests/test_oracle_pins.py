@@ -393,3 +393,20 @@ def test_workload_generator_is_deterministic_and_shaped():
     assert wl5.n_query_sample == 512 and wl5.d == 512
     b4 = wls.WORKLOADS["unet-lowres"]
     assert b4.dtype == "bf16" and b4.d == 64
+
+
+def test_step_functions_compose_to_the_block():
+    """The exported attention and output-projection steps, fed the oracle's
+    own Q/K/V and O, give the same branch as the full block (they are the
+    block's steps 3 and 4), and the attention step matches torch's SDPA."""
+    B, C, H, W, G, h = 2, 12, 3, 5, 3, 3
+    x = _x(B, C, H, W, 60)
+    p = _params(C, 61)
+    r = oracle.forward(x, p, G, h, want=("q", "k", "v", "o"))
+    o = oracle.attention(r["q"], r["k"], r["v"], h)
+    np.testing.assert_array_equal(o, r["o"])
+    y = oracle.out_proj(o, p["out_weight"], p["out_bias"])
+    np.testing.assert_array_equal(y, r["y"])
+    qt, kt, vt = (torch.from_numpy(r[n]).view(B, H * W, h, C // h).transpose(1, 2) for n in "qkv")
+    ref = F.scaled_dot_product_attention(qt, kt, vt).transpose(1, 2).reshape(B, H * W, C).numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
