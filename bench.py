@@ -1,0 +1,420 @@
+"""Benchmark of the spatial self-attention block forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path (GN statistics -> fused QKV GEMM ->
+flash attention -> output projection with residual) over one batch of seeded
+synthetic input, through the C ABI (ssa_forward_planned: the parameters are
+module constants packed once).  Timing: CUDA events on the launching stream
+around each step, L2 flushed (a 512 MB write) between steps outside the
+events, W >= 3 untimed warm-up steps, barrier + synchronize on both sides of
+the timed loop, max over ranks.  Multi-GPU: every rank runs an independent
+replica (the block has no exchange step), value = all ranks' pixel-tokens /
+max time ("weak" scaling).  Prints ONE JSON line on rank 0.
+
+--impl reference times the fp64 CPU oracle (the method as defined, plain
+loops) on this machine's host cores instead, on a bounded query sample of the
+same workload, extrapolated to the whole workload by the algorithmic FLOP
+ratio.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from diffusion_net_spatial_gb300 import workloads as wls  # noqa: E402
+
+METRIC = "block fwd pixel-tokens/s and TFLOP/s (% of GB300 dense bf16 peak), 1 GPU"
+UNIT = "pixel-tokens/s"
+DEFAULT_WORKLOAD = "vae16384"
+L2_FLUSH_BYTES = 512 << 20
+# A short device-side spin before each timed step lets the host enqueue the
+# whole step first, so the events time the kernels, not host launch gaps.
+HOST_LEAD_CYCLES = 400_000
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ ranks ---
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, seconds_this_rank: float, world: int) -> dict:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    t = max_over_ranks(seconds_this_rank, world)
+    return {"seconds": t, "value": tokens_per_rank * world / t}
+
+
+# ----------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ traffic file ---
+
+def kernel_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel_file}_{workload}.md")
+    src = os.path.join(ROOT, "diffusion_net_spatial_gb300", "csrc", f"{kernel_file}.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_b or m_src.group(1) != digest:
+        return None
+    return float(m_b.group(1))
+
+
+# ----------------------------------------------------------- CPU baseline ---
+
+def oracle_sample(wl, nq: int, seed: int = 0):
+    """Time the fp64 oracle on nq seeded query pixels of the workload (K and V
+    for every pixel), and extrapolate to the whole workload by the ratio of
+    algorithmic FLOPs.  Returns (seconds_measured, seconds_full_estimate)."""
+    import oracle
+    x, p, _ = wls.make_inputs(wl)
+    g = torch.Generator().manual_seed(seed)
+    qidx = torch.sort(torch.randperm(wl.N, generator=g)[:nq]).values.numpy()
+    xf = x.double().numpy()
+    pf = {k: v.double().numpy() for k, v in p.items()}
+    t0 = time.perf_counter()
+    oracle.forward(xf, pf, wl.num_groups, wl.num_heads, qidx=qidx)
+    dt = time.perf_counter() - t0
+    B, C, N = wl.B, wl.C, wl.N
+    f_sample = B * (4.0 * N * C * C + nq * (4.0 * C * C + 4.0 * N * C))
+    return dt, dt * wl.flops / f_sample
+
+
+def sample_size(wl, budget_flops: float = 4e11) -> int:
+    """Query sample for a bounded oracle run (seconds to tens of seconds on the host cores)."""
+    B, C, N = wl.B, wl.C, wl.N
+    per_q = B * (4.0 * C * C + 4.0 * N * C)
+    fixed = B * 4.0 * N * C * C
+    nq = int(max(16, (budget_flops - fixed) / per_q))
+    return min(N, nq)
+
+
+def cpu_baseline(wl) -> dict:
+    import oracle
+    nq = sample_size(wl)
+    dt, full = oracle_sample(wl, nq)
+    return {"value": wl.tokens / full, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{nq} seeded query pixels of {wl.name} (K,V for all {wl.N} pixels), {dt:.2f}s measured, "
+                      f"extrapolated to the whole workload by the algorithmic FLOP ratio"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on host cores (rank 0 only)."""
+    wl = wls.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    nq = sample_size(wl, budget_flops=1.2e12 / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(wl, 16)
+    est = []
+    meas = 0.0
+    for _ in range(args.steps):
+        dt, full = oracle_sample(wl, nq)
+        meas += dt
+        est.append(full)
+    t_step = statistics.mean(est)
+    value = wl.tokens / t_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, "oracle, query-sampled"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{nq} seeded query pixels per step (K,V for all pixels), {meas:.1f}s measured, "
+                                   f"extrapolated by the algorithmic FLOP ratio"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, mode: str) -> dict:
+    return {"workload": wl.name, "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W, "num_groups": wl.num_groups,
+            "num_heads": wl.num_heads, "x_dtype": wl.dtype, "mode": mode,
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)", "seed": wl.seed}
+
+
+# ---------------------------------------------------------------- our arm ---
+
+def run_ours(args, rank, world, local):
+    import diffusion_net_spatial_gb300 as ssa
+    wl = wls.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    peaks = load_peaks()
+    x, p, _ = wls.make_inputs(wl)
+    with torch.cuda.stream(stream):
+        xd = x.to(dev)
+        pd = {k: v.to(dev) for k, v in p.items()}
+        plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads, stream=stream)
+        out = torch.empty_like(xd)
+        ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        plan.forward(xd, out=out, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    st = ssa.ssa_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+
+    # ---- timed region: the whole block, one event pair per step
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                torch.cuda._sleep(HOST_LEAD_CYCLES)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    st = ssa.ssa_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(ms) / 1e3
+    agg = aggregate(wl.tokens * K, total_s, world)
+    ms_per_step = agg["seconds"] / K * 1e3
+    tflops = wl.flops * K * world / agg["seconds"] / 1e12
+
+    # ---- per-kernel breakdown (same kernels, launched step by step)
+    lay = ssa.layout(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
+    with torch.cuda.stream(stream):
+        pk = ssa.ssa_pack_weights(pd, wl.num_heads, stream=stream)
+    names = ["gn_stats", "qkv_gemm", "attention", "out_proj"]
+    per = {n: [] for n in names}
+    kb = max(3, min(K, 20))
+    with torch.cuda.stream(stream):
+        for i in range(kb + 2):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
+            _, _, a, s = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"], stream=stream)
+            ev[1].record(stream)
+            q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], wl.num_heads, stream=stream)
+            ev[2].record(stream)
+            o = ssa.ssa_attention(q, k, vt, wl.B, wl.C, wl.N, wl.num_heads, stream=stream)
+            ev[3].record(stream)
+            ssa.ssa_out_project(o, pk["w_o"], pk["b_o"], xd, out=out, stream=stream)
+            ev[4].record(stream)
+            if i >= 2:
+                per_i = ev
+                torch.cuda.synchronize(dev)
+                for j, n in enumerate(names):
+                    per[n].append(per_i[j].elapsed_time(per_i[j + 1]))
+    torch.cuda.synchronize(dev)
+    kern_ms = {n: statistics.mean(v) for n, v in per.items()}
+    B, C, N = wl.B, wl.C, wl.N
+    flops_k = {"gn_stats": 0.0, "qkv_gemm": 6.0 * B * N * C * C, "attention": 4.0 * B * N * N * C,
+               "out_proj": 2.0 * B * N * C * C}
+    dominant = max(kern_ms, key=kern_ms.get)
+    if dominant == "gn_stats":
+        achieved = B * C * N * (4 if wl.dtype == "f32" else 2) / (kern_ms[dominant] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = flops_k[dominant] / (kern_ms[dominant] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(dominant, wl.name)
+    roof["kernel"] = dominant
+    roof["peak_source"] = (f"{peaks['source']} bf16 dense burst (fp16 operands: same nominal tensor rate)"
+                           if roof["bound"] == "tensor" else f"{peaks['source']} HBM copy")
+
+    # ---- end to end through the public API with host buffers
+    x_host = x.pin_memory()
+    out_host = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    Ke = max(3, min(K, 20))
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    with torch.cuda.stream(stream):
+        xe = torch.empty_like(xd)
+        for i in range(Ke + 2):
+            flush.fill_(i & 0xFF)
+            j = i - 2
+            if j >= 0:
+                e0[j].record(stream)
+            xe.copy_(x_host, non_blocking=True)
+            plan.forward(xe, out=out, workspace=ws, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+            if j >= 0:
+                e1[j].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / 1e3
+    e2e = aggregate(wl.tokens * Ke, e2e_s, world)
+    xbytes = x.numel() * x.element_size()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": config_of(wl, "planned (parameters packed once), fp16 tensor-core operands, fp32 accumulate"),
+        "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
+        "pct_of_bf16_sustained_peak": tflops / peaks["bf16_tflops_sustained"],
+        "kernels_ms": kern_ms,
+        "roofline": roof,
+        "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
+        "gpu_launches": K * ssa.ssa_launches_per_forward(True),
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wls.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

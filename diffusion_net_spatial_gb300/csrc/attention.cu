@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int buf = j & 1;
-      if (!mbar_wait(&s_full[buf], (j >> 1) & 1, ab)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[buf], (j >> 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
@@ -255,14 +255,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < 32; ++i)
           if (32 * c + i < kvalid) mx = fmaxf(mx, __uint_as_float(r[c][i]));
       const float m_new = fmaxf(m_used, mx * sl2);
+      // Lazy rescale: a row raises its reference maximum only when the new
+      // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
+      // per warp (any row that needs it), because the tensor-memory accesses
+      // that rescale O are warp-collective; rows that did not need it use
+      // their own (possibly unit) factor.
+      const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
+      const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
       float alpha = 1.f;
-      bool rescale = false;
       if (j == 0) {
         m_used = m_new;
-      } else if (m_new > m_used + RESCALE_LOG2) {
+      } else if (rescale && m_new > m_used) {
         alpha = ex2_approx(m_used - m_new);
         m_used = m_new;
-        rescale = true;
       }
       const float neg_m = -m_used;
       float sum = 0.f;
@@ -278,8 +283,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           pk[(32 * c + i) >> 1] = pack_half2(e0, e1);
         }
       l = l * alpha + sum;
-      if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, ab)) { ok = false; break; }
+      if (j > 0 && !mbar_wait_warp(o_done, (j - 1) & 1, ab)) { ok = false; break; }
       if (rescale) {
+        __syncwarp();
         tc_fence_after();
         for (int cc = 0; cc < args.d_o / 16; ++cc) {
           uint32_t t[16];
@@ -301,7 +307,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(o_done, (n - 1) & 1, ab)) {
+    if (ok && mbar_wait_warp(o_done, (n - 1) & 1, ab)) {
+      __syncwarp();
       tc_fence_after();
       const float inv = 1.0f / l;
       const int b = bh / args.h, hd = bh % args.h;

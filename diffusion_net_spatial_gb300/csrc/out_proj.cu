@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    if (mbar_wait(acc_full, 0, ab)) {
+    if (mbar_wait_warp(acc_full, 0, ab)) {
+      __syncwarp();
       tc_fence_after();
       const int ew = warp - 2;
       const int q4 = warp & 3;

@@ -80,6 +80,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Warp-uniform form of mbar_wait: every lane waits, and the warp proceeds only
+// if all lanes saw the phase complete.  Used before .sync.aligned tcgen05
+// instructions, which must be executed by the whole warp or not at all.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const Abort &ab) {
+  const bool ok = mbar_wait(bar, parity, ab);
+  return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
 // Wait used only while cleaning up after an abort: bounded, never raises.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();

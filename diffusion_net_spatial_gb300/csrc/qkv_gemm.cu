@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int sx = kb % XST, s = kb % ST;
-      if (!mbar_wait(&x_full[sx], (kb / XST) & 1, ab)) { ok = false; break; }
-      if (kb >= ST && !mbar_wait(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) { ok = false; break; }
+      if (!mbar_wait_warp(&x_full[sx], (kb / XST) & 1, ab)) { ok = false; break; }
+      if (kb >= ST && !mbar_wait_warp(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) { ok = false; break; }
       const int c = kb * BK + hc * 32 + lane;
       __syncwarp();
       slot[lane] = c < args.C ? __ldg(ga + c) : 0.f;
@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(acc_full, 0, ab)) {
+    if (ok && mbar_wait_warp(acc_full, 0, ab)) {
+      __syncwarp();
       tc_fence_after();
       const int q4 = warp & 3;                // lane quarter this warp may read
       const int half = cw >> 2;

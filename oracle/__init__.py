@@ -72,8 +72,28 @@ def _load():
     lib.ssa_oracle_round.restype = None
     lib.ssa_oracle_num_threads.argtypes = []
     lib.ssa_oracle_num_threads.restype = ctypes.c_int
+    lib.ssa_oracle_set_num_threads.argtypes = [ctypes.c_int]
+    lib.ssa_oracle_set_num_threads.restype = None
+    lib.ssa_oracle_set_num_threads(usable_cpus())
     _lib = lib
     return lib
+
+
+def usable_cpus() -> int:
+    """CPUs this process may actually run on: the affinity mask, capped by a
+    cgroup CPU quota when one is set (so OpenMP does not oversubscribe)."""
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    try:
+        with open("/sys/fs/cgroup/cpu.max") as f:
+            quota, period = f.read().split()[:2]
+        if quota != "max":
+            n = min(n, max(1, int(int(quota) // int(period))))
+    except (OSError, ValueError):
+        pass
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit() and int(env) > 0:
+        n = int(env)
+    return max(1, n)
 
 
 def _dptr(a):

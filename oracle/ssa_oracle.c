@@ -276,12 +276,25 @@ void ssa_oracle_round(const double *v, long long n, int dtype, void *out)
     }
 }
 
+#ifdef _OPENMP
+extern int omp_get_max_threads(void);
+extern void omp_set_num_threads(int);
+#endif
+
 int ssa_oracle_num_threads(void)
 {
 #ifdef _OPENMP
-    extern int omp_get_max_threads(void);
     return omp_get_max_threads();
 #else
     return 1;
+#endif
+}
+
+void ssa_oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
 #endif
 }
