@@ -489,3 +489,78 @@ ssa_status ssa_debug_timeout_probe(uint64_t timeout_ns, void *stream) {
 }
 
 }  // extern "C"
+
+// ======================================================= allocation-free ==
+// ssa_forward_static: the same block as ssa_forward, for callers that cannot
+// allocate device memory -- code that runs where cudaMalloc is not allowed or
+// not wanted once set-up is over (a fixed-memory real-time or embedded
+// deployment, a plugin whose host forbids allocation on its execution path,
+// a caller without access to any device allocator).  Its scratch (packed
+// weights, GroupNorm scale/shift, Q, K, V^T, O) lives in one file-scope
+// device array of SSA_STATIC_WORKSPACE_BYTES, which every device that loads
+// this library's module keeps reserved until the process exits.
+namespace ssa {
+namespace {
+
+constexpr size_t kStaticWsBytes = SSA_STATIC_WORKSPACE_BYTES;
+__device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+uint8_t *g_static_ws_ptr[kMaxDevices] = {};
+
+// The array's name is only a host-side handle; its device address is looked
+// up once per device (with that device current) and cached.
+ssa_status static_workspace(uint8_t **ws) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SSA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+    g_static_ws_ptr[dev] = static_cast<uint8_t *>(p);
+  }
+  *ws = g_static_ws_ptr[dev];
+  return SSA_OK;
+}
+
+}  // namespace
+}  // namespace ssa
+
+extern "C" ssa_status ssa_forward_static(const void *x, int B, int C, int H, int W, int num_groups,
+                                         int num_heads, const void *norm_weight, const void *norm_bias,
+                                         const void *q_weight, const void *q_bias, const void *k_weight,
+                                         const void *k_bias, const void *v_weight, const void *v_bias,
+                                         const void *out_weight, const void *out_bias, void *out,
+                                         ssa_dtype dtype, void *stream) {
+  ssa_status s = check_shape(B, C, H, W, num_groups, num_heads);
+  if (s != SSA_OK) return s;
+  if ((s = check_dtype(dtype)) != SSA_OK) return s;
+  const void *ptrs[] = {x, norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias,
+                        v_weight, v_bias, out_weight, out_bias, out};
+  for (const void *p : ptrs)
+    if (!p) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if (!aligned16(x) || !aligned16(out)) return fail(SSA_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
+  const Dims dm = make_dims(B, C, H, W, num_groups, num_heads);
+  const WsLayout wl = ws_layout(dm, dtype, true);
+  if (wl.total > kStaticWsBytes)
+    return fail(SSA_ERR_WORKSPACE,
+                "this problem needs %zu bytes of scratch, above the %zu-byte built-in limit of "
+                "ssa_forward_static; call ssa_forward with a workspace instead",
+                wl.total, kStaticWsBytes);
+  KParams kp{};
+  int num_sms = 0;
+  if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
+  uint8_t *ws = nullptr;
+  if ((s = static_workspace(&ws)) != SSA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t *w_qkv = reinterpret_cast<uint16_t *>(ws + wl.wqkv);
+  float *b_qkv = reinterpret_cast<float *>(ws + wl.bqkv);
+  uint16_t *w_o = reinterpret_cast<uint16_t *>(ws + wl.wo);
+  float *b_o = reinterpret_cast<float *>(ws + wl.bo);
+  cudaError_t e = launch_pack_weights(dm, (int)dtype, q_weight, q_bias, k_weight, k_bias, v_weight, v_bias,
+                                      out_weight, out_bias, w_qkv, b_qkv, w_o, b_o, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  const Ptrs p{norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias, v_weight, v_bias, out_weight, out_bias};
+  return run_block(dm, dtype, x, out, p, w_qkv, b_qkv, w_o, b_o, ws, wl, kp, num_sms, st);
+}

@@ -93,6 +93,32 @@ ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H
                                void *workspace, size_t workspace_bytes, void *stream);
 void ssa_plan_destroy(ssa_plan *plan);
 
+/* Built-in scratch size of ssa_forward_static (48 MiB). */
+#define SSA_STATIC_WORKSPACE_BYTES ((size_t)48 << 20)
+
+/* Allocation-free form of ssa_forward, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is forbidden or unwanted after
+ * set-up (fixed-memory real-time or embedded deployments, plugins whose host
+ * bans allocation on the execution path, callers with no device allocator
+ * at hand).  The paper has no counterpart; it is a packaging of the same
+ * block.  Arguments and results are those of ssa_forward minus the
+ * workspace: the scratch is one library-owned device array of
+ * SSA_STATIC_WORKSPACE_BYTES, reserved on every device that loads the
+ * library until the process exits.  Problems whose ssa_workspace_size()
+ * exceeds it are rejected with SSA_ERR_WORKSPACE.  The first call on a
+ * device looks the array's address up (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Every call shares the one array and
+ * it keeps the last call's contents (nothing in it needs to start at zero),
+ * so calls whose work can overlap on the GPU -- on different streams, or from
+ * different threads -- race on it: order them on one stream. */
+ssa_status ssa_forward_static(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                              const void *norm_weight, const void *norm_bias,
+                              const void *q_weight, const void *q_bias,
+                              const void *k_weight, const void *k_bias,
+                              const void *v_weight, const void *v_bias,
+                              const void *out_weight, const void *out_bias,
+                              void *out, ssa_dtype dtype, void *stream);
+
 /* ------------------------------------------------- steps of the hot path --- *
  * Each step of the block as its own launch, with the library's internal
  * layouts, for per-step checks and timing.  Let
