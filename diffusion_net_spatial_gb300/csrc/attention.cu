@@ -5,19 +5,28 @@
 // d = 2).
 //
 // Flash-style: one CTA owns 128 queries of one (sample, head) -- and one of
-// the two 256-column halves of O when the padded head dim exceeds 256 -- and
-// walks the keys in tiles of 128, so the N x N score matrix never exists.
-//   warp 0     TMA producer: Q once, then K tiles and V^T tiles through a
-//              ring of 32 KB stages (128-byte swizzled K-major boxes)
-//   warp 1     tcgen05 MMA issuer: S = Q K^T into one of two tensor-memory
-//              score buffers, O += P V into a tensor-memory accumulator
-//   warps 2-5  softmax: one query row per thread.  Scores are read from
-//              tensor memory, the 1/sqrt(d) scale and log2(e) fold into one
-//              FFMA ahead of ex2, P is rounded to fp16 into a swizzled shared
-//              tile for the next MMA.  The running maximum is only raised
-//              (and O rescaled in tensor memory) when it grows by more than
-//              2^8, which keeps every P <= 256 and is exact after the final
+// the two output halves when the padded head dim exceeds 256 -- and walks the
+// keys in tiles of 128, so the N x N score matrix never exists.
+//   warp 0     TMA producer: Q once, then K and V^T through a ring of slots
+//              (16 KB with two CTAs per SM, 32 KB with one) of 128-byte
+//              swizzled, K-major boxes: K as [128 keys x 64 dims] per 16 KB,
+//              V^T as [<=256 output dims x 64 keys]
+//   warp 1     tcgen05 MMA issuer: S = Q K^T into tensor memory, O += P V into
+//              a tensor-memory accumulator
+//   warps 2-5  softmax: one query row per thread.  Scores come from tensor
+//              memory, the 1/sqrt(d) scale and log2(e) fold into one FFMA
+//              ahead of ex2, P is rounded to fp16 into a swizzled shared tile
+//              for the next MMA.  The running maximum is only raised (and O
+//              rescaled in tensor memory) when it grows by more than 2^8,
+//              which keeps every P <= 256 and is exact after the final
 //              division by the row sum.
+// Two score-buffer modes:
+//   single  S uses 128 tensor-memory columns; the MMA writes S_{j+1} as soon
+//           as the softmax warps have read S_j.  With a small head dim this
+//           fits 256 columns and ~113 KB of shared memory, so two CTAs share
+//           an SM and their softmax warpgroups overlap.
+//   double  S alternates between two 128-column buffers (512 columns in all,
+//           one CTA per SM); used when O needs more than 128 columns.
 // Keys past N in the last tile are zero-filled by TMA and masked to -inf.
 #include <cuda_fp16.h>
 
@@ -29,13 +38,14 @@ namespace {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int STAGE = 32768;
+constexpr int BLK = 16384;  // one [128 x 64] fp16 swizzled block
 constexpr int THREADS = 192;
-constexpr int MAX_SMEM = 232448;
+constexpr int MAX_SMEM_FALLBACK = 232448;
+constexpr int SM_SMEM_PER_TWO = 115712;  // per-CTA budget when two CTAs share an SM
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct AttnArgs {
-  int N, h, d, dp, ldc, d_o, n_oc, nqb, nkc, nvc, nst, ntiles;
+  int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
   float sl2;  // log2(e) / sqrt(d)
   uint16_t *o;
   uint32_t *err;
@@ -45,32 +55,36 @@ struct AttnArgs {
 struct Layout {
   uint32_t q, p, ring, bars;
 };
-__host__ __device__ inline Layout layout(int nqb, int nst) {
+__host__ __device__ inline Layout layout(int nqb, int nst, int slot) {
   Layout L;
   L.q = 0;
   L.p = nqb * 16384;
   L.ring = L.p + 32768;
-  L.bars = L.ring + nst * STAGE;
+  L.bars = L.ring + nst * slot;
   return L;
 }
-__host__ __device__ inline int nbars(int nst) { return 2 * nst + 6; }
-__host__ __device__ inline uint32_t smem_bytes(int nqb, int nst) {
-  return layout(nqb, nst).bars + nbars(nst) * 8 + 16 + 1024;
+// full[nst], empty[nst], q_full, s_full[2], s_free, p_full, o_done, drain
+__host__ __device__ inline int nbars(int nst) { return 2 * nst + 7; }
+__host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot) {
+  return layout(nqb, nst, slot).bars + nbars(nst) * 8 + 16 + 1024;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool SINGLE>
+__global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nst = args.nst;
-  const Layout L = layout(args.nqb, nst);
+  const int slot = args.slot;
+  const Layout L = layout(args.nqb, nst, slot);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
   uint64_t *full = bars;
   uint64_t *empty = bars + nst;
   uint64_t *q_full = bars + 2 * nst;
   uint64_t *s_full = q_full + 1;  // [2]
-  uint64_t *p_full = s_full + 2;
+  uint64_t *s_free = s_full + 2;
+  uint64_t *p_full = s_free + 1;
   uint64_t *o_done = p_full + 1;
   uint64_t *drain = o_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nbars(nst));
@@ -82,6 +96,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bh = blockIdx.y;
   const int q0 = qt * BQ;
   const int n = args.ntiles;
+  constexpr bool single = SINGLE;
+  const int nvb = 2 * args.nvr;                         // V slots per key tile
+  const int nks = (args.nqb + args.kpb - 1) / args.kpb;  // K slots per key tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
@@ -91,6 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(q_full, 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
+    mbar_init(s_free, 4);
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -101,7 +119,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&vmap);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, (uint32_t)args.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -109,10 +127,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, args.err, args.timeout_ns};
-  const uint32_t TM_O = 256;  // O accumulator columns [256, 256 + d_o)
+  const uint32_t TM_O = (uint32_t)args.o_col;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Block order (the MMA issuer consumes in the same order):
+    //   K(0), K(1), then for each tile j: V(j), K(j+2).
     if (lane == 0) {
       int it = 0;
       bool ok = true;
@@ -122,29 +142,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         return i < nst || mbar_wait(&empty[i % nst], ((i / nst) - 1) & 1, ab);
       };
       auto load_k = [&](int j) {
-        for (int kc = 0; kc < args.nkc && ok; ++kc) {
+        for (int ks = 0; ks < nks && ok; ++ks) {
           if (!acquire(it)) { ok = false; break; }
           const int s = it % nst;
-          const int nblk = min(2, args.nqb - 2 * kc);
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(nblk * 16384));
+          const int nblk = min(args.kpb, args.nqb - ks * args.kpb);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(nblk * BLK));
           for (int bl = 0; bl < nblk; ++bl)
-            tma_load_3d(sm + L.ring + s * STAGE + bl * 16384, &kmap, &full[s], (2 * kc + bl) * 64, j * BKV, bh);
+            tma_load_3d(sm + L.ring + s * slot + bl * BLK, &kmap, &full[s], (ks * args.kpb + bl) * 64, j * BKV, bh);
           ++it;
         }
       };
       auto load_v = [&](int j) {
-        for (int vc = 0; vc < args.nvc && ok; ++vc) {
+        for (int vb = 0; vb < nvb && ok; ++vb) {
           if (!acquire(it)) { ok = false; break; }
           const int s = it % nst;
-          uint8_t *dst = sm + L.ring + s * STAGE;
-          if (args.nvc == 1) {
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * args.d_o * 128));
-            tma_load_3d(dst, &vmap, &full[s], j * BKV, oc * args.d_o, bh);
-            tma_load_3d(dst + args.d_o * 128, &vmap, &full[s], j * BKV + 64, oc * args.d_o, bh);
-          } else {
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(args.d_o * 128));
-            tma_load_3d(dst, &vmap, &full[s], j * BKV + 64 * vc, oc * args.d_o, bh);
-          }
+          const int vh = vb / args.nvr, vr = vb % args.nvr;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(args.vrows * 128));
+          tma_load_3d(sm + L.ring + s * slot, &vmap, &full[s], j * BKV + 64 * vh, oc * args.d_o + vr * args.vrows, bh);
           ++it;
         }
       };
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_f16(BQ, BKV);
-      const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.d_o);
+      const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.vrows);
       const uint32_t q_addr = smem_u32(sm + L.q);
       const uint32_t p_addr = smem_u32(sm + L.p);
       const uint32_t ring = smem_u32(sm + L.ring);
@@ -172,18 +186,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       bool ok = true, issued = false;
       auto issue_s = [&](int buf) {
-        for (int kc = 0; kc < args.nkc && ok; ++kc) {
+        for (int ksl = 0; ksl < nks && ok; ++ksl) {
           const int s = it % nst;
           if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
           tc_fence_after();
-          const int nblk = min(2, args.nqb - 2 * kc);
+          const int nblk = min(args.kpb, args.nqb - ksl * args.kpb);
           for (int bl = 0; bl < nblk; ++bl) {
-            const int qb = 2 * kc + bl;
+            const int kb = ksl * args.kpb + bl;
             for (int kk = 0; kk < 4; ++kk) {
-              const int ks = qb * 4 + kk;
+              const int ks = kb * 4 + kk;
               if (ks >= ksteps) break;
-              mma_f16_ss(tmem + (uint32_t)(buf * BKV), sdesc_k128(q_addr + qb * 16384 + kk * 32),
-                         sdesc_k128(ring + s * STAGE + bl * 16384 + kk * 32), idesc_s, ks > 0 ? 1u : 0u);
+              mma_f16_ss(tmem + (uint32_t)(buf * BKV), sdesc_k128(q_addr + kb * 16384 + kk * 32),
+                         sdesc_k128(ring + s * slot + bl * BLK + kk * 32), idesc_s, ks > 0 ? 1u : 0u);
             }
           }
           mma_commit(&empty[s]);
@@ -193,18 +207,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (ok) mma_commit(&s_full[buf]);
       };
       auto issue_pv = [&](int j) {
-        for (int vc = 0; vc < args.nvc && ok; ++vc) {
+        for (int vb = 0; vb < nvb && ok; ++vb) {
           const int s = it % nst;
           if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
           tc_fence_after();
-          const int h0 = args.nvc == 1 ? 0 : vc;
-          const int h1 = args.nvc == 1 ? 2 : vc + 1;
-          for (int vh = h0; vh < h1; ++vh) {
-            const uint32_t vaddr = ring + s * STAGE + (args.nvc == 1 ? vh * args.d_o * 128 : 0);
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(tmem + TM_O, sdesc_k128(p_addr + vh * 16384 + kk * 32), sdesc_k128(vaddr + kk * 32),
-                         idesc_o, (j > 0 || vh > 0 || kk > 0) ? 1u : 0u);
-          }
+          const int vh = vb / args.nvr, vr = vb % args.nvr;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss(tmem + TM_O + (uint32_t)(vr * args.vrows), sdesc_k128(p_addr + vh * 16384 + kk * 32),
+                       sdesc_k128(ring + s * slot + kk * 32), idesc_o, (j > 0 || vh > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
           issued = true;
           ++it;
@@ -215,13 +225,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        if (n > 1) issue_s(1);
       }
       for (int j = 0; j < n && ok; ++j) {
-        if (!mbar_wait(p_full, j & 1, ab)) { ok = false; break; }
+        if (single) {
+          if (j + 1 < n) {
+            if (!mbar_wait(s_free, j & 1, ab)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(0);
+          }
+        } else if (j == 0 && n > 1) {
+          issue_s(1);
+        }
+        if (!ok || !mbar_wait(p_full, j & 1, ab)) { ok = false; break; }
         tc_fence_after();
         issue_pv(j);
-        if (j + 2 < n) issue_s(j & 1);
+        if (!single && j + 2 < n) issue_s(j & 1);
       }
       if (!ok && issued) {
         mma_commit(drain);
@@ -240,20 +258,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
-      if (!mbar_wait_warp(&s_full[buf], (j >> 1) & 1, ab)) { ok = false; break; }
+      const int buf = single ? 0 : (j & 1);
+      const uint32_t par = single ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+      if (!mbar_wait_warp(&s_full[buf], par, ab)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + (uint32_t)(buf * BKV + 32 * c), r[c]);
       tmem_wait_ld();
+      if (single) {
+        // S has been read into registers: the MMA may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+      }
       const int kvalid = min(BKV, args.N - j * BKV);
-      float mx = -INFINITY;
+      if (kvalid < BKV) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
+      }
+      float pm[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) pm[t] = __uint_as_float(r[t >> 1][(t & 1) * 16]);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (32 * c + i < kvalid) mx = fmaxf(mx, __uint_as_float(r[c][i]));
+        for (int i = 0; i < 16; ++i) {
+          pm[2 * c] = fmaxf(pm[2 * c], __uint_as_float(r[c][i]));
+          pm[2 * c + 1] = fmaxf(pm[2 * c + 1], __uint_as_float(r[c][16 + i]));
+        }
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float m_new = fmaxf(m_used, mx * sl2);
       // Lazy rescale: a row raises its reference maximum only when the new
       // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
@@ -270,18 +308,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_used = m_new;
       }
       const float neg_m = -m_used;
-      float sum = 0.f;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int kidx = 32 * c + i;
-          const float e0 = kidx < kvalid ? ex2_approx(fmaf(__uint_as_float(r[c][i]), sl2, neg_m)) : 0.f;
-          const float e1 = kidx + 1 < kvalid ? ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), sl2, neg_m)) : 0.f;
-          sum += e0 + e1;
+          const float e0 = ex2_approx(fmaf(__uint_as_float(r[c][i]), sl2, neg_m));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), sl2, neg_m));
+          ps[(2 * c + (i >> 4)) & 7] += e0 + e1;
           pk[(32 * c + i) >> 1] = pack_half2(e0, e1);
         }
+      const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + sum;
       if (j > 0 && !mbar_wait_warp(o_done, (j - 1) & 1, ab)) { ok = false; break; }
       if (rescale) {
@@ -349,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
   }
 }
 
@@ -357,6 +395,40 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
                      const KParams &kp, cudaStream_t st) {
+  AttnArgs a{};
+  a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
+  a.nqb = (dm.dp + 63) / 64;
+  a.ntiles = (dm.N + BKV - 1) / BKV;
+  int max_smem = MAX_SMEM_FALLBACK, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  // Two CTAs per SM (16 KB slots) when O fits 128 columns and the ring still
+  // has >= 2 slots; otherwise one CTA per SM with 32 KB slots.
+  int nst = (int)(((long long)SM_SMEM_PER_TWO - (long long)smem_bytes(a.nqb, 0, BLK)) / (BLK + 16));
+  if (dm.d_o <= 128 && nst >= 2) {
+    a.single = 1;
+    a.tmem_cols = 256;
+    a.o_col = 128;
+    a.slot = BLK;
+    if (nst > 3) nst = 3;
+  } else {
+    a.single = 0;
+    a.tmem_cols = 512;
+    a.o_col = 256;
+    a.slot = 2 * BLK;
+    nst = (int)(((long long)max_smem - (long long)smem_bytes(a.nqb, 0, a.slot)) / (a.slot + 16));
+    if (nst > 6) nst = 6;
+  }
+  a.kpb = a.slot / BLK;
+  a.vrows = dm.d_o <= a.slot / 128 ? dm.d_o : a.slot / 128;
+  a.nvr = (dm.d_o + a.vrows - 1) / a.vrows;
+  if (nst < 2) return 2;
+  a.nst = nst;
+  a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
+  a.o = o;
+  a.err = kp.err;
+  a.timeout_ns = kp.timeout_ns;
+
   CUtensorMap qmap, kmap, vmap;
   const uint64_t BH = (uint64_t)dm.B * dm.h;
   {
@@ -373,32 +445,20 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   {
     const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, BH};
     const uint64_t strides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
-    const uint32_t box[3] = {64, (uint32_t)dm.d_o, 1};
+    const uint32_t box[3] = {64, (uint32_t)a.vrows, 1};
     if (encode_tiled(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  AttnArgs a{};
-  a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
-  a.nqb = (dm.dp + 63) / 64;
-  a.nkc = (a.nqb + 1) / 2;
-  a.nvc = dm.d_o <= 128 ? 1 : 2;
-  a.ntiles = (dm.N + BKV - 1) / BKV;
-  int max_smem = MAX_SMEM, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int nst = (int)(((long long)max_smem - (long long)smem_bytes(a.nqb, 0)) / (STAGE + 16));
-  if (nst > 6) nst = 6;
-  if (nst < 2) return 2;
-  a.nst = nst;
-  a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
-  a.o = o;
-  a.err = kp.err;
-  a.timeout_ns = kp.timeout_ns;
-  const uint32_t smem = smem_bytes(a.nqb, nst);
-  cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const uint32_t smem = smem_bytes(a.nqb, nst, a.slot);
   const dim3 grid((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
-  attention_kernel<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+  if (a.single) {
+    cudaFuncSetAttribute(attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attention_kernel<true><<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+  } else {
+    cudaFuncSetAttribute(attention_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attention_kernel<false><<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 

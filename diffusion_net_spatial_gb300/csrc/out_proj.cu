@@ -137,20 +137,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
         tmem_wait_ld();
         if (!valid) continue;
+        // All residual reads of the chunk are issued before any store: out
+        // may alias x, so interleaving them would serialise every load
+        // behind the previous store.
+        const int cbase = n0 + c16 * 16;
+        const int nc = min(16, args.C - cbase);
+        const long long idx0 = ((long long)b * args.C + cbase) * plane + p;
+        float xv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int c = n0 + c16 * 16 + i;
-          if (c >= args.C) break;
-          const long long idx = ((long long)b * args.C + c) * plane + p;
-          const float y = __uint_as_float(r[i]) + __ldg(args.bias + c);
-          if (DT == 0) {
-            const float xv = reinterpret_cast<const float *>(args.x)[idx];
-            reinterpret_cast<float *>(args.out)[idx] = xv + y;
-          } else {
-            const unsigned short xb = reinterpret_cast<const unsigned short *>(args.x)[idx];
-            const float xv = __uint_as_float(((uint32_t)xb) << 16);
-            const __nv_bfloat16 ov = __float2bfloat16_rn(xv + y);
-            reinterpret_cast<__nv_bfloat16 *>(args.out)[idx] = ov;
+          if (i < nc) {
+            if (DT == 0) {
+              xv[i] = reinterpret_cast<const float *>(args.x)[idx0 + i * plane];
+            } else {
+              const unsigned short xb = reinterpret_cast<const unsigned short *>(args.x)[idx0 + i * plane];
+              xv[i] = __uint_as_float(((uint32_t)xb) << 16);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i < nc) {
+            const float v = xv[i] + (__uint_as_float(r[i]) + __ldg(args.bias + cbase + i));
+            if (DT == 0) {
+              reinterpret_cast<float *>(args.out)[idx0 + i * plane] = v;
+            } else {
+              reinterpret_cast<__nv_bfloat16 *>(args.out)[idx0 + i * plane] = __float2bfloat16_rn(v);
+            }
           }
         }
       }

@@ -174,14 +174,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float *ga = args.ga + (long long)b * args.C;
     const float *gs = args.gs + (long long)b * args.C;
     bool ok = true;
+    // The GN scale/shift of the next k-block are fetched one iteration ahead,
+    // so their global-memory latency overlaps the current block.
+    int c = hc * 32 + lane;
+    float a_cur = c < args.C ? __ldg(ga + c) : 0.f;
+    float s_cur = c < args.C ? __ldg(gs + c) : 0.f;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int sx = kb % XST, s = kb % ST;
+      c = (kb + 1) * BK + hc * 32 + lane;
+      const float a_nxt = (kb + 1 < nk && c < args.C) ? __ldg(ga + c) : 0.f;
+      const float s_nxt = (kb + 1 < nk && c < args.C) ? __ldg(gs + c) : 0.f;
       if (!mbar_wait_warp(&x_full[sx], (kb / XST) & 1, ab)) { ok = false; break; }
       if (kb >= ST && !mbar_wait_warp(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) { ok = false; break; }
-      const int c = kb * BK + hc * 32 + lane;
       __syncwarp();
-      slot[lane] = c < args.C ? __ldg(ga + c) : 0.f;
-      slot[32 + lane] = c < args.C ? __ldg(gs + c) : 0.f;
+      slot[lane] = a_cur;
+      slot[32 + lane] = s_cur;
+      a_cur = a_nxt;
+      s_cur = s_nxt;
       __syncwarp();
       const uint8_t *xs = sm + L.xs + sx * args.xbytes;
       const uint32_t a_tile = smem_u32(sm + L.as + s * (BM * BK * 2));
