@@ -46,6 +46,7 @@ constexpr float RESCALE_LOG2 = 8.0f;
 
 struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
+  int p_tmem, p_col;  // P in tensor memory (and its column in single mode) or in shared memory
   float sl2;  // log2(e) / sqrt(d)
   uint16_t *o;
   uint32_t *err;
@@ -55,18 +56,18 @@ struct AttnArgs {
 struct Layout {
   uint32_t q, p, ring, bars;
 };
-__host__ __device__ inline Layout layout(int nqb, int nst, int slot) {
+__host__ __device__ inline Layout layout(int nqb, int nst, int slot, int p_tmem) {
   Layout L;
   L.q = 0;
   L.p = nqb * 16384;
-  L.ring = L.p + 32768;
+  L.ring = L.p + (p_tmem ? 0 : 32768);
   L.bars = L.ring + nst * slot;
   return L;
 }
 // full[nst], empty[nst], q_full, s_full[2], s_free, p_full, o_done, drain
 __host__ __device__ inline int nbars(int nst) { return 2 * nst + 7; }
-__host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot) {
-  return layout(nqb, nst, slot).bars + nbars(nst) * 8 + 16 + 1024;
+__host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot, int p_tmem) {
+  return layout(nqb, nst, slot, p_tmem).bars + nbars(nst) * 8 + 16 + 1024;
 }
 
 template <bool SINGLE>
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nst = args.nst;
   const int slot = args.slot;
-  const Layout L = layout(args.nqb, nst, slot);
+  const Layout L = layout(args.nqb, nst, slot, args.p_tmem);
+  const bool p_tmem = args.p_tmem != 0;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
   uint64_t *full = bars;
   uint64_t *empty = bars + nst;
@@ -134,32 +136,33 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     // Block order (the MMA issuer consumes in the same order):
     //   K(0), K(1), then for each tile j: V(j), K(j+2).
     if (lane == 0) {
-      int it = 0;
+      int it = 0, s = 0;
+      uint32_t ph = 0;  // parity of the ring round of slot s
       bool ok = true;
       mbar_arrive_expect_tx(q_full, (uint32_t)(args.nqb * 16384));
       for (int qb = 0; qb < args.nqb; ++qb) tma_load_3d(sm + L.q + qb * 16384, &qmap, q_full, qb * 64, q0, bh);
-      auto acquire = [&](int i) -> bool {
-        return i < nst || mbar_wait(&empty[i % nst], ((i / nst) - 1) & 1, ab);
+      auto acquire = [&]() -> bool { return it < nst || mbar_wait(&empty[s], ph ^ 1u, ab); };
+      auto advance = [&]() {
+        ++it;
+        if (++s == nst) { s = 0; ph ^= 1u; }
       };
       auto load_k = [&](int j) {
         for (int ks = 0; ks < nks && ok; ++ks) {
-          if (!acquire(it)) { ok = false; break; }
-          const int s = it % nst;
+          if (!acquire()) { ok = false; break; }
           const int nblk = min(args.kpb, args.nqb - ks * args.kpb);
           mbar_arrive_expect_tx(&full[s], (uint32_t)(nblk * BLK));
           for (int bl = 0; bl < nblk; ++bl)
             tma_load_3d(sm + L.ring + s * slot + bl * BLK, &kmap, &full[s], (ks * args.kpb + bl) * 64, j * BKV, bh);
-          ++it;
+          advance();
         }
       };
       auto load_v = [&](int j) {
         for (int vb = 0; vb < nvb && ok; ++vb) {
-          if (!acquire(it)) { ok = false; break; }
-          const int s = it % nst;
-          const int vh = vb / args.nvr, vr = vb % args.nvr;
+          if (!acquire()) { ok = false; break; }
+          const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
           mbar_arrive_expect_tx(&full[s], (uint32_t)(args.vrows * 128));
           tma_load_3d(sm + L.ring + s * slot, &vmap, &full[s], j * BKV + 64 * vh, oc * args.d_o + vr * args.vrows, bh);
-          ++it;
+          advance();
         }
       };
       load_k(0);
@@ -176,48 +179,67 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are formed once; a K step (32 B) or a 1024-B block offset
+    // inside the swizzled tiles is a small add to the start-address field.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_f16(BQ, BKV);
       const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.vrows);
-      const uint32_t q_addr = smem_u32(sm + L.q);
-      const uint32_t p_addr = smem_u32(sm + L.p);
-      const uint32_t ring = smem_u32(sm + L.ring);
+      const uint64_t qd = sdesc_k128(smem_u32(sm + L.q));
+      const uint64_t pd = sdesc_k128(smem_u32(sm + L.p));
+      const uint64_t rd = sdesc_k128(smem_u32(sm + L.ring));
+      const uint32_t slot16 = (uint32_t)slot >> 4;
       const int ksteps = args.dp / 16;
-      int it = 0;
+      int s = 0;
+      uint32_t ph = 0;
       bool ok = true, issued = false;
+      auto advance = [&]() {
+        if (++s == nst) { s = 0; ph ^= 1u; }
+      };
       auto issue_s = [&](int buf) {
+        const uint32_t d_s = tmem + (uint32_t)(buf * BKV);
         for (int ksl = 0; ksl < nks && ok; ++ksl) {
-          const int s = it % nst;
-          if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
           tc_fence_after();
+          const uint64_t bd = rd + (uint64_t)(s * slot16);
           const int nblk = min(args.kpb, args.nqb - ksl * args.kpb);
           for (int bl = 0; bl < nblk; ++bl) {
             const int kb = ksl * args.kpb + bl;
-            for (int kk = 0; kk < 4; ++kk) {
-              const int ks = kb * 4 + kk;
-              if (ks >= ksteps) break;
-              mma_f16_ss(tmem + (uint32_t)(buf * BKV), sdesc_k128(q_addr + kb * 16384 + kk * 32),
-                         sdesc_k128(ring + s * slot + bl * BLK + kk * 32), idesc_s, ks > 0 ? 1u : 0u);
-            }
+            const uint64_t a0 = qd + (uint64_t)(kb * 1024);
+            const uint64_t b0 = bd + (uint64_t)(bl * 1024);
+            const int kmax = min(4, ksteps - kb * 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              if (kk < kmax) mma_f16_ss(d_s, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_s, (kb | kk) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           issued = true;
-          ++it;
+          advance();
         }
         if (ok) mma_commit(&s_full[buf]);
       };
       auto issue_pv = [&](int j) {
+        const uint32_t pcol = single ? (uint32_t)args.p_col : (uint32_t)((j & 1) * BKV);
         for (int vb = 0; vb < nvb && ok; ++vb) {
-          const int s = it % nst;
-          if (!mbar_wait(&full[s], (it / nst) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
           tc_fence_after();
-          const int vh = vb / args.nvr, vr = vb % args.nvr;
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(tmem + TM_O + (uint32_t)(vr * args.vrows), sdesc_k128(p_addr + vh * 16384 + kk * 32),
-                       sdesc_k128(ring + s * slot + kk * 32), idesc_o, (j > 0 || vh > 0 || kk > 0) ? 1u : 0u);
+          const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
+          const uint32_t d_o = tmem + TM_O + (uint32_t)(vr * args.vrows);
+          const uint64_t b0 = rd + (uint64_t)(s * slot16);
+          const uint32_t first = (j > 0 || vh > 0) ? 1u : 0u;
+          if (p_tmem) {
+            const uint32_t a0 = tmem + pcol + (uint32_t)(vh * 32);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts(d_o, a0 + (uint32_t)(kk * 8), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+          } else {
+            const uint64_t a0 = pd + (uint64_t)(vh * 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+          }
           mma_commit(&empty[s]);
           issued = true;
-          ++it;
+          advance();
         }
         if (ok) mma_commit(o_done);
       };
@@ -280,18 +302,17 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
+      // Row maximum: eight independent 3-input max chains.
       float pm[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) pm[t] = __uint_as_float(r[t >> 1][(t & 1) * 16]);
+      for (int t = 0; t < 8; ++t) {
+        const int c = t >> 1, o = (t & 1) * 16;
+        float m = __uint_as_float(r[c][o]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          pm[2 * c] = fmaxf(pm[2 * c], __uint_as_float(r[c][i]));
-          pm[2 * c + 1] = fmaxf(pm[2 * c + 1], __uint_as_float(r[c][16 + i]));
-        }
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
+        pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
+      }
+      const float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       const float m_new = fmaxf(m_used, mx * sl2);
       // Lazy rescale: a row raises its reference maximum only when the new
       // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
@@ -307,19 +328,27 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
         alpha = ex2_approx(m_used - m_new);
         m_used = m_new;
       }
-      const float neg_m = -m_used;
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
+      // p = 2^(s * log2(e)/sqrt(d) - m): one paired FMA per two scores, the
+      // row sum in four paired accumulators.
+      const uint64_t c2 = f2_pack(sl2, sl2);
+      const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(r[c][i]), sl2, neg_m));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(r[c][i + 1]), sl2, neg_m));
-          ps[(2 * c + (i >> 4)) & 7] += e0 + e1;
-          pk[(32 * c + i) >> 1] = pack_half2(e0, e1);
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+          const float e0 = ex2_approx(t0);
+          const float e1 = ex2_approx(t1);
+          acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
+          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_half2(e0, e1);
         }
-      const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      float s0, s1, s2, s3;
+      f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+      f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
+      const float sum = (s0 + s1) + (s2 + s3);
       l = l * alpha + sum;
       if (j > 0 && !mbar_wait_warp(o_done, (j - 1) & 1, ab)) { ok = false; break; }
       if (rescale) {
@@ -335,11 +364,22 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
         }
         tmem_wait_st();
       }
+      if (p_tmem) {
+        // P as fp16 pairs in tensor memory: over the S buffer just read
+        // (double) or in its own 64 columns (single).
+        const uint32_t pcol = single ? (uint32_t)args.p_col : (uint32_t)(buf * BKV);
+        __syncwarp();
+        tmem_st32(lane_base + pcol, pk[0]);
+        tmem_st32(lane_base + pcol + 32, pk[1]);
+        tmem_wait_st();
+      } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(p_tile + (c >> 3) * 16384 + sw128_offset((uint32_t)row, (uint32_t)(c & 7)), pk[4 * c],
-                     pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(p_tile + (c >> 3) * 16384 + sw128_offset((uint32_t)row, (uint32_t)(c & 7)),
+                       pk[c >> 3][(4 * c) & 31], pk[c >> 3][(4 * c + 1) & 31], pk[c >> 3][(4 * c + 2) & 31],
+                       pk[c >> 3][(4 * c + 3) & 31]);
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
@@ -402,21 +442,29 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  // Two CTAs per SM (16 KB slots) when O fits 128 columns and the ring still
-  // has >= 2 slots; otherwise one CTA per SM with 32 KB slots.
-  int nst = (int)(((long long)SM_SMEM_PER_TWO - (long long)smem_bytes(a.nqb, 0, BLK)) / (BLK + 16));
+  // Two CTAs per SM (16 KB slots, 256 TMEM columns) when the O slice fits 128
+  // columns and the ring still has >= 2 slots; P then lives in its own 64
+  // TMEM columns when the O slice fits 64 (else in shared memory).  Otherwise
+  // one CTA per SM, 32 KB slots, two S buffers, P over the S buffer it
+  // replaces.
+  const int p_tmem_single = dm.d_o <= 64 ? 1 : 0;
+  int nst = (int)(((long long)SM_SMEM_PER_TWO - (long long)smem_bytes(a.nqb, 0, BLK, p_tmem_single)) / (BLK + 16));
   if (dm.d_o <= 128 && nst >= 2) {
     a.single = 1;
     a.tmem_cols = 256;
-    a.o_col = 128;
+    a.p_tmem = p_tmem_single;
+    a.p_col = 128;
+    a.o_col = p_tmem_single ? 192 : 128;
     a.slot = BLK;
-    if (nst > 3) nst = 3;
+    if (nst > 4) nst = 4;
   } else {
     a.single = 0;
     a.tmem_cols = 512;
+    a.p_tmem = 1;
+    a.p_col = 0;
     a.o_col = 256;
     a.slot = 2 * BLK;
-    nst = (int)(((long long)max_smem - (long long)smem_bytes(a.nqb, 0, a.slot)) / (a.slot + 16));
+    nst = (int)(((long long)max_smem - (long long)smem_bytes(a.nqb, 0, a.slot, 1)) / (a.slot + 16));
     if (nst > 6) nst = 6;
   }
   a.kpb = a.slot / BLK;
@@ -450,7 +498,7 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  const uint32_t smem = smem_bytes(a.nqb, nst, a.slot);
+  const uint32_t smem = smem_bytes(a.nqb, nst, a.slot, a.p_tmem);
   const dim3 grid((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
   if (a.single) {
     cudaFuncSetAttribute(attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
