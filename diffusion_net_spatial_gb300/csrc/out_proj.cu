@@ -4,14 +4,20 @@
 //
 // One CTA computes a 128-pixel x BN-channel tile (M = pixels of one sample,
 // N = output channels, K = C):
-//   warp 0      TMA producer: O tile [128 pixels][64 channels] and Wo tile
-//               [BN][64] (fp16, 128-byte swizzle, K-major)
+//   warp 0      TMA producer: the residual tile x[b, n0:n0+BN, p0:p0+128]
+//               (NCHW, x's dtype) once, then the O tile [128 pixels][64
+//               channels] and the Wo tile [BN][64] per K step (fp16,
+//               128-byte swizzle, K-major)
 //   warp 1      tcgen05 MMA issuer, fp32 accumulator in tensor memory
-//   warps 2..9  epilogue: tensor-memory lane = pixel, column = channel, so for
-//               each channel a warp reads 32 consecutive pixels of x and
-//               writes 32 consecutive pixels of out -- the residual read, the
-//               bias add, the single rounding to x's dtype and the transposed
-//               NCHW store are one coalesced pass.
+//   warps 2..9  epilogue: tensor-memory lane = pixel, column = channel.  Each
+//               thread adds its accumulator row and the bias into the staged
+//               residual tile in place (x + y, one rounding to x's dtype);
+//               one thread then writes the whole tile back to out with a
+//               single TMA store, which clips at the image and channel edges.
+// When a channel row of x is not a whole number of 16-byte units (H*W*sizeof
+// not a multiple of 16) TMA cannot address it, and the epilogue reads x and
+// writes out directly instead (all reads of a chunk before its writes: out
+// may alias x).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -27,7 +33,7 @@ constexpr int NEPI = 8;
 constexpr int THREADS = (2 + NEPI) * 32;
 
 struct OutArgs {
-  int C, N, BN, nk, tmem_cols;
+  int C, N, BN, nk, tmem_cols, tma_epi, es;
   const float *bias;
   const void *x;
   void *out;
@@ -35,23 +41,34 @@ struct OutArgs {
   uint64_t timeout_ns;
 };
 
-__host__ __device__ inline uint32_t bars_off(int BN) { return ST * (BM * BK * 2 + BN * BK * 2); }
-constexpr int NBARS = 2 * ST + 2;
-__host__ __device__ inline uint32_t smem_total(int BN) { return bars_off(BN) + NBARS * 8 + 16 + 1024; }
+__host__ __device__ inline uint32_t xs_off(int BN) { return ST * (BM * BK * 2 + BN * BK * 2); }
+__host__ __device__ inline uint32_t bars_off(int BN, int tma_epi, int es) {
+  return xs_off(BN) + (tma_epi ? (uint32_t)(BN * BM * es) : 0u);
+}
+// full[ST], empty[ST], acc_full, drain, x_full, epi_done
+constexpr int NBARS = 2 * ST + 4;
+__host__ __device__ inline uint32_t smem_total(int BN, int tma_epi, int es) {
+  return bars_off(BN, tma_epi, es) + NBARS * 8 + 16 + 1024;
+}
 
 template <int DT>
 __global__ void __launch_bounds__(THREADS, 1)
     out_proj_kernel(const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap wmap,
+                    const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap outmap,
                     const OutArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = args.BN;
+  const bool tma_epi = args.tma_epi != 0;
   const uint32_t a_off = 0, b_off = ST * (BM * BK * 2);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + bars_off(BN));
+  uint8_t *xs = sm + xs_off(BN);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + bars_off(BN, args.tma_epi, args.es));
   uint64_t *full = bars;
   uint64_t *empty = bars + ST;
   uint64_t *acc_full = bars + 2 * ST;
   uint64_t *drain = acc_full + 1;
+  uint64_t *x_full = drain + 1;
+  uint64_t *epi_done = x_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -68,10 +85,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    mbar_init(x_full, 1);
+    mbar_init(epi_done, NEPI);
     *abort_flag = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&omap);
     tma_prefetch_desc(&wmap);
+    if (tma_epi) {
+      tma_prefetch_desc(&xmap);
+      tma_prefetch_desc(&outmap);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, (uint32_t)args.tmem_cols);
@@ -85,6 +108,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      if (tma_epi) {
+        mbar_arrive_expect_tx(x_full, (uint32_t)(BN * BM * args.es));
+        tma_load_3d(xs, &xmap, x_full, p0, n0, b);
+      }
       int it = 0;
       const uint32_t bytes = (uint32_t)(BM * BK * 2 + BN * BK * 2);
       for (; it < nk; ++it) {
@@ -95,22 +122,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d(sm + b_off + s * (BN * BK * 2), &wmap, &full[s], it * BK, n0);
       }
       for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_wait_drain(&full[i % ST], (i / ST) & 1, ab.limit_ns);
+      if (tma_epi) mbar_wait_drain(x_full, 0, ab.limit_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(BM, (uint32_t)BN);
+      const uint64_t ad = sdesc_k128(smem_u32(sm + a_off));
+      const uint64_t bd = sdesc_k128(smem_u32(sm + b_off));
       bool ok = true, issued = false;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % ST;
         if (!mbar_wait(&full[s], (kb / ST) & 1, ab)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(sm + a_off + s * (BM * BK * 2));
-        const uint32_t b_addr = smem_u32(sm + b_off + s * (BN * BK * 2));
+        const uint64_t a0 = ad + (uint64_t)((s * (BM * BK * 2)) >> 4);
+        const uint64_t b0 = bd + (uint64_t)((s * (BN * BK * 2)) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16_ss(tmem, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+          mma_f16_ss(tmem, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
         mma_commit(&empty[s]);
         issued = true;
       }
@@ -122,47 +151,80 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    if (mbar_wait_warp(acc_full, 0, ab)) {
+    const int ew = warp - 2;
+    const int q4 = warp & 3;
+    const int half = ew >> 2;
+    const int row = q4 * 32 + lane;
+    const int p = p0 + row;
+    bool ok = mbar_wait_warp(acc_full, 0, ab);
+    if (ok && tma_epi) ok = mbar_wait_warp(x_full, 0, ab);
+    if (ok) {
       __syncwarp();
       tc_fence_after();
-      const int ew = warp - 2;
-      const int q4 = warp & 3;
-      const int half = ew >> 2;
-      const int row = q4 * 32 + lane;
-      const int p = p0 + row;
-      const bool valid = p < args.N;
-      const long long plane = (long long)args.N;
-      for (int c16 = half; c16 < BN / 16; c16 += 2) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
-        tmem_wait_ld();
-        if (!valid) continue;
-        // All residual reads of the chunk are issued before any store: out
-        // may alias x, so interleaving them would serialise every load
-        // behind the previous store.
-        const int cbase = n0 + c16 * 16;
-        const int nc = min(16, args.C - cbase);
-        const long long idx0 = ((long long)b * args.C + cbase) * plane + p;
-        float xv[16];
+      if (tma_epi) {
+        // In place over the staged residual tile xs[channel][pixel].
+        for (int c16 = half; c16 < BN / 16; c16 += 2) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (i < nc) {
+          for (int i = 0; i < 16; ++i) {
+            const int cl = c16 * 16 + i;
+            const int c = n0 + cl;
+            const float bias = c < args.C ? __ldg(args.bias + c) : 0.f;
             if (DT == 0) {
-              xv[i] = reinterpret_cast<const float *>(args.x)[idx0 + i * plane];
+              float *px = reinterpret_cast<float *>(xs) + cl * BM + row;
+              *px = *px + (__uint_as_float(r[i]) + bias);
             } else {
-              const unsigned short xb = reinterpret_cast<const unsigned short *>(args.x)[idx0 + i * plane];
-              xv[i] = __uint_as_float(((uint32_t)xb) << 16);
+              __nv_bfloat16 *px = reinterpret_cast<__nv_bfloat16 *>(xs) + cl * BM + row;
+              const float xv = __bfloat162float(*px);
+              *px = __float2bfloat16_rn(xv + (__uint_as_float(r[i]) + bias));
             }
           }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_done);
+        if (ew == 0 && lane == 0 && mbar_wait(epi_done, 0, ab)) {
+          tma_store_3d(&outmap, xs, p0, n0, b);
+          tma_store_commit();
+          tma_store_wait_all();
+        }
+      } else {
+        const bool valid = p < args.N;
+        const long long plane = (long long)args.N;
+        for (int c16 = half; c16 < BN / 16; c16 += 2) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
+          tmem_wait_ld();
+          if (!valid) continue;
+          // All residual reads of the chunk are issued before any store: out
+          // may alias x, so interleaving them would serialise every load
+          // behind the previous store.
+          const int cbase = n0 + c16 * 16;
+          const int nc = min(16, args.C - cbase);
+          const long long idx0 = ((long long)b * args.C + cbase) * plane + p;
+          float xv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (i < nc) {
-            const float v = xv[i] + (__uint_as_float(r[i]) + __ldg(args.bias + cbase + i));
-            if (DT == 0) {
-              reinterpret_cast<float *>(args.out)[idx0 + i * plane] = v;
-            } else {
-              reinterpret_cast<__nv_bfloat16 *>(args.out)[idx0 + i * plane] = __float2bfloat16_rn(v);
+          for (int i = 0; i < 16; ++i) {
+            if (i < nc) {
+              if (DT == 0) {
+                xv[i] = reinterpret_cast<const float *>(args.x)[idx0 + i * plane];
+              } else {
+                const unsigned short xb = reinterpret_cast<const unsigned short *>(args.x)[idx0 + i * plane];
+                xv[i] = __uint_as_float(((uint32_t)xb) << 16);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (i < nc) {
+              const float v = xv[i] + (__uint_as_float(r[i]) + __ldg(args.bias + cbase + i));
+              if (DT == 0) {
+                reinterpret_cast<float *>(args.out)[idx0 + i * plane] = v;
+              } else {
+                reinterpret_cast<__nv_bfloat16 *>(args.out)[idx0 + i * plane] = __float2bfloat16_rn(v);
+              }
             }
           }
         }
@@ -178,9 +240,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-int pick_bn(int C) {
+int pick_bn(int C, int cap) {
   const int c16 = (C + 15) / 16 * 16;
-  for (int bn = 256; bn >= 16; bn -= 16)
+  for (int bn = cap; bn >= 16; bn -= 16)
     if (c16 % bn == 0) return bn;
   return 16;
 }
@@ -189,8 +251,13 @@ int pick_bn(int C) {
 
 int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t *w_o, const float *b_o,
                     const void *x, void *out, const KParams &kp, cudaStream_t st) {
-  CUtensorMap omap, wmap;
-  const int BN = pick_bn(dm.C);
+  const int es = dtype == 0 ? 4 : 2;
+  const int tma_epi = ((long long)dm.N * es) % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                              (reinterpret_cast<uintptr_t>(out) & 15u) == 0
+                          ? 1
+                          : 0;
+  const int BN = pick_bn(dm.C, tma_epi ? 128 : 256);
+  CUtensorMap omap, wmap, xmap, outmap;
   {
     const uint64_t dims[3] = {(uint64_t)dm.C, (uint64_t)dm.N, (uint64_t)dm.B};
     const uint64_t strides[2] = {(uint64_t)dm.ldc * 2, (uint64_t)dm.N * dm.ldc * 2};
@@ -207,18 +274,30 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
+  if (tma_epi) {
+    const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.C, (uint64_t)dm.B};
+    const uint64_t strides[2] = {(uint64_t)dm.N * es, (uint64_t)dm.C * dm.N * es};
+    const uint32_t box[3] = {BM, (uint32_t)BN, 1};
+    const CUtensorMapDataType dt = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (encode_tiled(&xmap, dt, 3, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS) return 1;
+    if (encode_tiled(&outmap, dt, 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS) return 1;
+  } else {
+    xmap = omap;  // unused
+    outmap = omap;
+  }
   OutArgs a{};
   a.C = dm.C; a.N = dm.N; a.BN = BN; a.nk = (dm.C + BK - 1) / BK;
   a.tmem_cols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  a.tma_epi = tma_epi; a.es = es;
   a.bias = b_o; a.x = x; a.out = out; a.err = kp.err; a.timeout_ns = kp.timeout_ns;
-  const uint32_t smem = smem_total(BN);
+  const uint32_t smem = smem_total(BN, tma_epi, es);
   const dim3 grid((dm.C + BN - 1) / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(out_proj_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    out_proj_kernel<0><<<grid, THREADS, smem, st>>>(omap, wmap, a);
+    out_proj_kernel<0><<<grid, THREADS, smem, st>>>(omap, wmap, xmap, outmap, a);
   } else {
     cudaFuncSetAttribute(out_proj_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    out_proj_kernel<1><<<grid, THREADS, smem, st>>>(omap, wmap, a);
+    out_proj_kernel<1><<<grid, THREADS, smem, st>>>(omap, wmap, xmap, outmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

@@ -58,8 +58,8 @@ __host__ __device__ inline Smem smem_layout(int xbytes, int BN) {
   s.bars = s.slot + NCONV * 256;
   return s;
 }
-// barriers: x_full[XST], x_empty[XST], b_full[ST], a_full[ST], ab_empty[ST], acc_full, drain
-constexpr int NBARS = 2 * XST + 3 * ST + 2;
+// barriers: x_full[XST], x_empty[XST], b_full[ST], a_full[ST], ab_empty[ST], acc_full, drain, epi_done
+constexpr int NBARS = 2 * XST + 3 * ST + 3;
 __host__ __device__ inline uint32_t smem_total(int xbytes, int BN) {
   return smem_layout(xbytes, BN).bars + NBARS * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
 }
@@ -67,7 +67,8 @@ __host__ __device__ inline uint32_t smem_total(int xbytes, int BN) {
 template <int DT>
 __global__ void __launch_bounds__(THREADS, 1)
     qkv_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                    const QkvArgs args) {
+                    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const QkvArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Smem L = smem_layout(args.xbytes, args.BN);
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *ab_empty = a_full + ST;
   uint64_t *acc_full = ab_empty + ST;
   uint64_t *drain = acc_full + 1;
+  uint64_t *epi_done = drain + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -100,10 +102,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    mbar_init(epi_done, NCONV);
     *abort_flag = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&xmap);
     tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, (uint32_t)args.tmem_cols);
@@ -220,45 +226,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     // ------------------------------------------------------------ epilogue
+    // The output tile is staged in the (now idle) operand ring in global
+    // order, one 4 KB chunk per 16 features: Q/K chunks as [128 pixels][16]
+    // (rows of the q/k layout), V chunks as [16][128 pixels] (rows of the
+    // transposed v layout).  One thread then stores each chunk with TMA,
+    // which clips pixels past N.
     if (ok && mbar_wait_warp(acc_full, 0, ab)) {
       __syncwarp();
       tc_fence_after();
       const int q4 = warp & 3;                // lane quarter this warp may read
       const int half = cw >> 2;
       const int row = q4 * 32 + lane;
-      const int p = p0 + row;
-      const bool valid = p < args.N;
       const int hdp = args.h * args.dp;
+      uint8_t *stage = sm + L.as;
       for (int c16 = half; c16 < args.BN / 16; c16 += 2) {
         uint32_t r[16];
         tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
         tmem_wait_ld();
         const int f0 = n0 + c16 * 16;
         const int sec = f0 / hdp;
-        const int hd = (f0 / args.dp) % args.h;
-        const int e0 = f0 % args.dp;
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + __ldg(args.bias + f0 + i);
-        if (!valid) continue;
-        const long long bh = (long long)b * args.h + hd;
+        uint8_t *chunk = stage + c16 * 4096;
         if (sec < 2) {
-          uint16_t *dst = (sec == 0 ? args.q : args.k) + (bh * args.N + p) * args.ldq + e0;
           uint4 w0, w1;
           w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
           w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
           w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
           w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
-          reinterpret_cast<uint4 *>(dst)[0] = w0;
-          reinterpret_cast<uint4 *>(dst)[1] = w1;
+          reinterpret_cast<uint4 *>(chunk + row * 32)[0] = w0;
+          reinterpret_cast<uint4 *>(chunk + row * 32)[1] = w1;
         } else {
-          uint16_t *dst = args.vt + (bh * args.dp + e0) * args.ldn + p;
+          __half *vt_rows = reinterpret_cast<__half *>(chunk);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __half hv = __float2half_rn(v[i]);
-            dst[(long long)i * args.ldn] = *reinterpret_cast<const uint16_t *>(&hv);
-          }
+          for (int i = 0; i < 16; ++i) vt_rows[i * BM + row] = __float2half_rn(v[i]);
         }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_done);
+      if (cw == 0 && lane == 0 && mbar_wait(epi_done, 0, ab)) {
+        for (int c16 = 0; c16 < args.BN / 16; ++c16) {
+          const int f0 = n0 + c16 * 16;
+          const int sec = f0 / hdp;
+          const int hd = (f0 / args.dp) % args.h;
+          const int e0 = f0 % args.dp;
+          const int bh = b * args.h + hd;
+          const uint8_t *chunk = stage + c16 * 4096;
+          if (sec == 0) tma_store_3d(&qmap, chunk, e0, p0, bh);
+          else if (sec == 1) tma_store_3d(&kmap, chunk, e0, p0, bh);
+          else tma_store_3d(&vmap, chunk, p0, e0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_all();
       }
     }
   }
@@ -302,6 +323,25 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
+  CUtensorMap qmap, kmap, vmap;
+  {
+    const uint64_t BH = (uint64_t)dm.B * dm.h;
+    const uint64_t dims[3] = {(uint64_t)dm.ldq, (uint64_t)dm.N, BH};
+    const uint64_t strides[2] = {(uint64_t)dm.ldq * 2, (uint64_t)dm.N * dm.ldq * 2};
+    const uint32_t box[3] = {16, BM, 1};
+    if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return 1;
+    if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return 1;
+    const uint64_t vdims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, BH};
+    const uint64_t vstrides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
+    const uint32_t vbox[3] = {BM, 16, 1};
+    if (encode_tiled(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, vdims, vstrides, vbox,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return 1;
+  }
   QkvArgs a{};
   a.C = dm.C; a.N = dm.N; a.h = dm.h; a.dp = dm.dp; a.ldq = dm.ldq; a.ldn = dm.ldn; a.BN = BN;
   a.nk = (dm.C + BK - 1) / BK;
@@ -313,10 +353,10 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
   const dim3 grid(dm.ntot / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(qkv_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_gemm_kernel<0><<<grid, THREADS, smem, st>>>(xmap, wmap, a);
+    qkv_gemm_kernel<0><<<grid, THREADS, smem, st>>>(xmap, wmap, qmap, kmap, vmap, a);
   } else {
     cudaFuncSetAttribute(qkv_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_gemm_kernel<1><<<grid, THREADS, smem, st>>>(xmap, wmap, a);
+    qkv_gemm_kernel<1><<<grid, THREADS, smem, st>>>(xmap, wmap, qmap, kmap, vmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
