@@ -9,7 +9,7 @@ namespace ssa {
 
 // Bits of the device error flag (one word per device, read and cleared by
 // the host); kernels receive its address as an argument.
-enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_MISALIGNED = 2 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

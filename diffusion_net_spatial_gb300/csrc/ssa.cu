@@ -474,6 +474,8 @@ ssa_status ssa_get_device_status(void *stream) {
     e = cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
     if (v & DEV_TIMEOUT) return fail(SSA_ERR_TIMEOUT, "a bounded device wait expired (error word 0x%x)", v);
+    if (v & DEV_MISALIGNED)
+      return fail(SSA_ERR_CUDA, "a kernel found its shared memory misaligned and did not run (error word 0x%x)", v);
     return fail(SSA_ERR_CUDA, "device error word 0x%x", v);
   }
   return SSA_OK;
