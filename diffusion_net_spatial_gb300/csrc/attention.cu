@@ -20,13 +20,15 @@
 //              rescaled in tensor memory) when it grows by more than 2^8,
 //              which keeps every P <= 256 and is exact after the final
 //              division by the row sum.
-// Two score-buffer modes:
+// Three modes:
 //   single  S uses 128 tensor-memory columns; the MMA writes S_{j+1} as soon
 //           as the softmax warps have read S_j.  With a small head dim this
 //           fits 256 columns and ~113 KB of shared memory, so two CTAs share
 //           an SM and their softmax warpgroups overlap.
 //   double  S alternates between two 128-column buffers (512 columns in all,
 //           one CTA per SM); used when O needs more than 128 columns.
+//   pair    padded head dim 512: a two-CTA cluster splits scores+softmax and
+//           P V between two SMs (described at attention_pair_kernel).
 // Keys past N in the last tile are zero-filled by TMA and masked to -inf.
 #include <cuda_fp16.h>
 
@@ -48,6 +50,8 @@ struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
   int p_tmem, p_col;  // P in tensor memory (and its column in single mode) or in shared memory
   float sl2;  // log2(e) / sqrt(d)
+  int ldq;             // pair mode: row pitch of Q, K (elements)
+  const uint16_t *q;   // pair mode: Q read directly into tensor memory
   uint16_t *o;
   uint32_t *err;
   uint64_t timeout_ns;
@@ -433,340 +437,452 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
 
 
 // ---------------------------------------------------------------------------
-// Wide mode (padded head dim 512, O in two 256-column halves over two CTAs):
-// every MMA has N = 256 -- score tiles of 256 keys and a 256-wide P V --
-// because on this GPU a stream that mixes MMA widths runs every MMA at the
-// N = 256 cadence (the two-buffer kernel above mixes N = 128 scores with an
-// N = 256 P V and is capped near half the tensor rate).  Tensor memory holds
-// one 256-column score buffer and the 256-column O half; P (fp16, 256 keys)
-// overwrites the first 128 columns of the scores it came from, so the score
-// MMA of the next tile is issued after P V.  Eight softmax warps: warp
-// (q4, half) owns 32 query rows and 128 of the 256 keys; the two halves of a
-// row exchange their maxima through shared memory and combine their sums at
-// the end.
-constexpr int BKW = 256;
-constexpr int WSLOT = 32768;
-__host__ __device__ inline uint32_t wide_ring_off() { return 8u * 16384u; }  // after Q (128 x 512 fp16)
-__host__ __device__ inline uint32_t wide_xch_off(int nst) { return wide_ring_off() + nst * WSLOT; }
-__host__ __device__ inline uint32_t wide_bars_off(int nst) { return wide_xch_off(nst) + 2048u; }
-// full[nst], empty[nst], q_full, s_full, p_full, o_done, drain, xbar[4]
-__host__ __device__ inline int wide_nbars(int nst) { return 2 * nst + 9; }
-__host__ __device__ inline uint32_t wide_smem(int nst) { return wide_bars_off(nst) + wide_nbars(nst) * 8 + 16; }
+// Pair mode (padded head dim 512).  O for 128 queries fills all 512 tensor-
+// memory columns, so one CTA cannot hold O and the scores at once.  A cluster
+// of two CTAs on two SMs shares one query tile and splits the work by role,
+// so the scores are computed once:
+//   rank 0 (score CTA)   Q (128 x 512, fp16) in tensor-memory columns
+//                        256..511; S_j = Q K_j^T for 128 keys (A operand from
+//                        tensor memory, N = 128) into one of two 128-column
+//                        score buffers, so S_{j+1} runs while the softmax
+//                        reads S_j.  Eight softmax warps (warp (q4, half): 32
+//                        rows x 64 keys) round P_j to fp16 into a local
+//                        swizzled staging tile; each warp then pushes its 4 KB
+//                        to the output CTA with one bulk shared-to-shared
+//                        copy, and the per-row rescale factors follow by
+//                        st.async -- all completing one barrier there.
+//   rank 1 (output CTA)  O (128 x 512 fp32) in all 512 columns; O += P_j V_j
+//                        as two groups of N = 256 MMAs (P from shared memory,
+//                        two buffers; V^T through a ring); four warps apply
+//                        the rare rescales to O before P_j V_j; at the end
+//                        O / l is written out.
+// Two producer warps per CTA issue the TMA loads (alternate ring slots): one
+// issuing thread cannot keep a ring of 32 KB boxes busy on this GPU.
+constexpr int PK = 128;          // keys per tile
+constexpr int PSLOT = 32768;     // ring slot: 32 KB of swizzled K or V^T blocks
+constexpr int PNST = 5;          // ring slots
+constexpr int PTHREADS = 352;    // warps: 0, 10 producers; 1 MMA; 2-9 softmax / rescale + epilogue
+constexpr uint32_t P_RING = 65536;                   // after the P area (two 32 KB tiles)
+constexpr uint32_t P_SMALL = P_RING + PNST * PSLOT;  // 2 KB: xch (rank 0) | alpha, flags, lsum (rank 1)
+constexpr uint32_t P_ALPHA = P_SMALL;                // [2 buffers][128] f32
+constexpr uint32_t P_FLAGS = P_SMALL + 1024;         // [2 buffers][4 quarters] u32
+constexpr uint32_t P_LSUM = P_SMALL + 1088;          // [128] f32
+constexpr uint32_t P_BARS = P_SMALL + 2048;
+enum {
+  PB_FULL = 0, PB_EMPTY = PB_FULL + PNST, PB_QREADY = PB_EMPTY + PNST, PB_SFULL = PB_QREADY + 1,
+  PB_SFREE = PB_SFULL + 2, PB_PFREE = PB_SFREE + 2, PB_XBAR = PB_PFREE + 2, PB_PFULL = PB_XBAR + 4,
+  PB_OREADY = PB_PFULL + 2, PB_PVDONE = PB_OREADY + 2, PB_LFULL = PB_PVDONE + 2, PB_OFINAL = PB_LFULL + 1,
+  PB_DRAIN = PB_OFINAL + 1, PB_COUNT = PB_DRAIN + 1
+};
+constexpr uint32_t P_SMEM = P_BARS + PB_COUNT * 8 + 16;
+constexpr uint32_t PMSG_BYTES = 32768 + 512 + 16;  // P tile + alpha + flags per key tile
 
-__global__ void __launch_bounds__(320, 1)
-    attention_wide_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
+    attention_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const AttnArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
   // The layout needs a 1024-byte aligned base (128B-swizzled operands) and
-  // leaves no room to realign: refuse to run otherwise.
+  // leaves no room to realign.  The base is the same in every CTA of the
+  // launch, so both CTAs of a cluster leave here together.
   if ((smem_u32(sm) & 1023u) != 0u) {
     if (threadIdx.x == 0) atomicOr(args.err, (uint32_t)DEV_MISALIGNED);
     return;
   }
-  const int nst = args.nst;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + wide_bars_off(nst));
-  uint64_t *full = bars;
-  uint64_t *empty = bars + nst;
-  uint64_t *q_full = bars + 2 * nst;
-  uint64_t *s_full = q_full + 1;
-  uint64_t *p_full = s_full + 1;
-  uint64_t *o_done = p_full + 1;
-  uint64_t *drain = o_done + 1;
-  uint64_t *xbar = drain + 1;  // [4]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + wide_nbars(nst));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P_BARS);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + P_BARS + PB_COUNT * 8);
   volatile uint32_t *abort_flag = tmem_slot + 1;
-  float *xch = reinterpret_cast<float *>(sm + wide_xch_off(nst));  // [2 parity][2 half][128]
-
+  const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x >> 1;
-  const int oc = blockIdx.x & 1;
+  const int q0 = (int)(blockIdx.x >> 1) * BQ;
   const int bh = blockIdx.y;
-  const int q0 = qt * BQ;
-  const int n = (args.N + BKW - 1) / BKW;
-  const int nqb = args.nqb;  // 64-wide blocks of the head dim (8)
+  const int n = (args.N + PK - 1) / PK;
+  const int nloads = n * 4;  // ring loads per CTA: 4 x 32 KB per key tile
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < PNST; ++i) {
+      mbar_init(&bars[PB_FULL + i], 1);
+      mbar_init(&bars[PB_EMPTY + i], 1);
     }
-    mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 8);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);
+    mbar_init(&bars[PB_QREADY], 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[PB_SFULL + b], 1);
+      mbar_init(&bars[PB_SFREE + b], 8);
+      mbar_init(&bars[PB_PFREE + b], 1);
+      mbar_init(&bars[PB_PFULL + b], 1);
+      mbar_init(&bars[PB_OREADY + b], 4);
+      mbar_init(&bars[PB_PVDONE + b], 1);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[PB_XBAR + i], 2);
+    mbar_init(&bars[PB_LFULL], 1);
+    mbar_init(&bars[PB_OFINAL], 1);
+    mbar_init(&bars[PB_DRAIN], 1);
     *abort_flag = 0u;
     fence_barrier_init();
-    tma_prefetch_desc(&qmap);
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
+    if (rank == 1) {
+      // Armed for the first two key tiles and for the row sums; the bytes
+      // come from the score CTA.
+      mbar_arrive_expect_tx(&bars[PB_PFULL + 0], PMSG_BYTES);
+      if (n > 1) mbar_arrive_expect_tx(&bars[PB_PFULL + 1], PMSG_BYTES);
+      mbar_arrive_expect_tx(&bars[PB_LFULL], 512u);
+      tma_prefetch_desc(&vmap);
+    } else {
+      tma_prefetch_desc(&kmap);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, args.err, args.timeout_ns};
-  const uint32_t TM_O = 256;
+  const uint32_t slot16 = (uint32_t)PSLOT >> 4;
 
-  if (warp == 0) {
-    // Block order: K(0) [nqb slots], then per tile j: V(j) [4 slots], K(j+1).
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------ TMA producers
+    // Load t goes to slot t mod PNST; warp 0 issues the even loads, warp 10
+    // the odd ones.  Rank 0: K as [2 x 64 dims] x 128 keys per load (4 per
+    // key tile); rank 1: V^T as [256 output dims x 64 keys] (output half 0,
+    // then half 1, two key blocks each).
     if (lane == 0) {
-      int it = 0, s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      mbar_arrive_expect_tx(q_full, (uint32_t)(nqb * 16384));
-      for (int qb = 0; qb < nqb; ++qb) tma_load_3d(sm + qb * 16384, &qmap, q_full, qb * 64, q0, bh);
-      auto acquire = [&]() -> bool { return it < nst || mbar_wait(&empty[s], ph ^ 1u, ab); };
-      auto advance = [&]() {
-        ++it;
-        if (++s == nst) { s = 0; ph ^= 1u; }
-      };
-      auto load_k = [&](int j) {
-        for (int kb = 0; kb < nqb && ok; ++kb) {
-          if (!acquire()) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], (uint32_t)WSLOT);
-          tma_load_3d(sm + wide_ring_off() + s * WSLOT, &kmap, &full[s], kb * 64, j * BKW, bh);
-          advance();
-        }
-      };
-      auto load_v = [&](int j) {
-        for (int vb = 0; vb < BKW / 64 && ok; ++vb) {
-          if (!acquire()) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], (uint32_t)WSLOT);
-          tma_load_3d(sm + wide_ring_off() + s * WSLOT, &vmap, &full[s], j * BKW + 64 * vb, oc * 256, bh);
-          advance();
-        }
-      };
-      load_k(0);
-      for (int j = 0; j < n && ok; ++j) {
-        load_v(j);
-        if (j + 1 < n) load_k(j + 1);
+      const int me = warp == 0 ? 0 : 1;
+      int last = -1;
+      for (int t = me; t < nloads; t += 2) {
+        const int s = t % PNST, round = t / PNST;
+        if (round > 0 && !mbar_wait(&bars[PB_EMPTY + s], (uint32_t)((round - 1) & 1), ab)) break;
+        mbar_arrive_expect_tx(&bars[PB_FULL + s], (uint32_t)PSLOT);
+        const int j = t >> 2, r = t & 3;
+        if (rank == 0)
+          tma_load_4d(sm + P_RING + s * PSLOT, &kmap, &bars[PB_FULL + s], 0, j * PK, 2 * r, bh);
+        else
+          tma_load_3d(sm + P_RING + s * PSLOT, &vmap, &bars[PB_FULL + s], j * PK + (r & 1) * 64, (r >> 1) * 256, bh);
+        last = t;
       }
-      mbar_wait_drain(q_full, 0, ab.limit_ns);
-      for (int i = (it > nst ? it - nst : 0); i < it; ++i)
-        mbar_wait_drain(&full[i % nst], (i / nst) & 1, ab.limit_ns);
+      // After an abort no load may still be landing when the CTA leaves.
+      if (*abort_flag)
+        for (int t = last; t >= 0 && t > last - 2 * PNST; t -= 2)
+          mbar_wait_drain(&bars[PB_FULL + t % PNST], (uint32_t)((t / PNST) & 1), ab.limit_ns);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(BQ, 256);
-      const uint64_t qd = sdesc_k128(smem_u32(sm));
-      const uint64_t rd = sdesc_k128(smem_u32(sm + wide_ring_off()));
-      const uint32_t slot16 = (uint32_t)WSLOT >> 4;
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true, issued = false;
-      auto advance = [&]() {
-        if (++s == nst) { s = 0; ph ^= 1u; }
-      };
-      if (!mbar_wait(q_full, 0, ab)) ok = false;
-      if (ok) tc_fence_after();
-      for (int j = 0; j < n && ok; ++j) {
-        // S_j = Q K_j^T (N = 256 keys).  Issued after P V_{j-1}, which reads
-        // the P that S_j overwrites (MMAs of one thread execute in order).
-        for (int kb = 0; kb < nqb && ok; ++kb) {
-          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
+  } else if (rank == 0) {
+    // ===================================================== score CTA ======
+    if (warp == 1) {
+      if (lane == 0) {
+        const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING));
+        const uint32_t idesc = idesc_f16(BQ, PK);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = mbar_wait(&bars[PB_QREADY], 0, ab), issued = false;
+        for (int j = 0; j < n && ok; ++j) {
+          const int buf = j & 1, u = j >> 1;
+          if (j >= 2 && !mbar_wait(&bars[PB_SFREE + buf], (uint32_t)((u - 1) & 1), ab)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t a0 = qd + (uint64_t)(kb * 1024);
-          const uint64_t b0 = rd + (uint64_t)(s * slot16);
+          const uint32_t d_s = tmem + (uint32_t)(buf * PK);
+          for (int c = 0; c < 4 && ok; ++c) {
+            if (!mbar_wait(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t b0 = rd + (uint64_t)(s * slot16);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(tmem, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (kb | kk) ? 1u : 0u);
-          mma_commit(&empty[s]);
-          issued = true;
-          advance();
+            for (int ks = 0; ks < 8; ++ks)  // 16 dims per step; Q dims 2c' and 2c'+1 in column 256 + c'
+              mma_f16_ts(d_s, tmem + 256u + (uint32_t)((c * 8 + ks) * 8), b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                         idesc, (c | ks) ? 1u : 0u);
+            mma_commit(&bars[PB_EMPTY + s]);
+            issued = true;
+            if (++s == PNST) { s = 0; ph ^= 1u; }
+          }
+          if (ok) mma_commit(&bars[PB_SFULL + buf]);
         }
-        if (!ok) break;
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, j & 1, ab)) { ok = false; break; }
-        tc_fence_after();
-        // O += P_j V_j: P in tensor memory, key k in column k/2.
-        for (int vb = 0; vb < BKW / 64 && ok; ++vb) {
-          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t b0 = rd + (uint64_t)(s * slot16);
-          const uint32_t first = (j > 0 || vb > 0) ? 1u : 0u;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ts(tmem + TM_O, tmem + (uint32_t)(vb * 32 + kk * 8), b0 + (uint64_t)(kk * 2), idesc,
-                       (first | kk) ? 1u : 0u);
-          mma_commit(&empty[s]);
-          issued = true;
-          advance();
+        if (!ok && issued) {
+          mma_commit(&bars[PB_DRAIN]);
+          mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
         }
-        if (ok) mma_commit(o_done);
       }
-      if (!ok && issued) {
-        mma_commit(drain);
-        mbar_wait_drain(drain, 0, ab.limit_ns);
-      }
-    }
-    __syncwarp();
-  } else {
-    const int sw = warp - 2;
-    const int q4 = warp & 3;
-    const int half = sw >> 2;
-    const int row = q4 * 32 + lane;
-    const int query = q0 + row;
-    const int cb = half * 128;  // this thread's 128 keys of the 256-key tile
-    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    const float sl2 = args.sl2;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!mbar_wait_warp(s_full, (uint32_t)(j & 1), ab)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + (uint32_t)(cb + 32 * c), r[c]);
-      tmem_wait_ld();
-      const int kvalid = min(BKW, args.N - j * BKW) - cb;
-      if (kvalid < 128) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
-      }
-      float pm[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = t >> 1, o = (t & 1) * 16;
-        float m = __uint_as_float(r[c][o]);
-#pragma unroll
-        for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
-        pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
-      }
-      float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      // The other half of this row (same lanes, other warp): exchange maxima.
-      // This also orders both halves' score reads before either writes P
-      // over the score columns.
-      xch[((j & 1) * 2 + half) * 128 + row] = mx;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[q4]);
-      if (!mbar_wait_warp(&xbar[q4], (uint32_t)(j & 1), ab)) { ok = false; break; }
-      mx = fmaxf(mx, xch[((j & 1) * 2 + (half ^ 1)) * 128 + row]);
-      const float m_new = fmaxf(m_used, mx * sl2);
-      const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
-      const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
-      float alpha = 1.f;
-      if (j == 0) {
-        m_used = m_new;
-      } else if (rescale && m_new > m_used) {
-        alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-      }
-      const uint64_t c2 = f2_pack(sl2, sl2);
-      const uint64_t nm2 = f2_pack(-m_used, -m_used);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
+    } else {
+      const int q4 = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      const float sl2 = args.sl2;
+      float *xch = reinterpret_cast<float *>(sm + P_SMALL);  // [2 parity][2 half][128]
+      const uint32_t r_base = mapa_u32(smem_u32(sm), 1u);
+      const uint32_t r_alpha = mapa_u32(smem_u32(sm + P_ALPHA), 1u);
+      const uint32_t r_flags = mapa_u32(smem_u32(sm + P_FLAGS), 1u);
+      const uint32_t r_lsum = mapa_u32(smem_u32(sm + P_LSUM), 1u);
+      const uint32_t r_pfull0 = mapa_u32(smem_u32(&bars[PB_PFULL]), 1u);
+      const uint32_t r_lfull = mapa_u32(smem_u32(&bars[PB_LFULL]), 1u);
+      {
+        // Q rows into tensor memory: this warp's 32 rows, dims half*256 ..
+        // +255 (rows past N are zero).
+        const bool qv = q0 + row < args.N;
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(
+            args.q + ((long long)bh * args.N + (qv ? q0 + row : 0)) * args.ldq + half * 256);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-          const float e0 = ex2_approx(t0);
-          const float e1 = ex2_approx(t1);
-          acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
-          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_half2(e0, e1);
-        }
-      float s0, s1, s2, s3;
-      f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
-      f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
-      l = l * alpha + ((s0 + s1) + (s2 + s3));
-      if (j > 0 && !mbar_wait_warp(o_done, (j - 1) & 1, ab)) { ok = false; break; }
-      if (rescale) {
-        __syncwarp();
-        tc_fence_after();
-        for (int cc = half; cc < 16; cc += 2) {
-          uint32_t t[16];
-          tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-          tmem_st16(lane_base + TM_O + (uint32_t)(cc * 16), t);
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = qv ? __ldg(qrow + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+          }
+          tmem_st32(lane_base + 256u + (uint32_t)(half * 128 + c * 32), w);
         }
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[PB_QREADY]);
+      }
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int buf = j & 1, u = j >> 1;
+        if (!mbar_wait_warp(&bars[PB_SFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[2][32];
+        tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64), r[0]);
+        tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64 + 32), r[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[PB_SFREE + buf]);
+        const int kvalid = min(PK, args.N - j * PK) - half * 64;
+        if (kvalid < 64) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
+        }
+        float pm[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = t >> 1, o = (t & 1) * 16;
+          float m = __uint_as_float(r[c][o]);
+#pragma unroll
+          for (int i = 1; i < 15; i += 2)
+            m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
+          pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
+        }
+        float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
+        // The other half of this row (same lanes, other warp): exchange maxima.
+        xch[((j & 1) * 2 + half) * 128 + row] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
+        if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(j & 1), ab)) { ok = false; break; }
+        mx = fmaxf(mx, xch[((j & 1) * 2 + (half ^ 1)) * 128 + row]);
+        const float m_new = fmaxf(m_used, mx * sl2);
+        const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
+        const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
+        float alpha = 1.f;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (rescale && m_new > m_used) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+        }
+        const uint64_t c2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-m_used, -m_used);
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+            const float e0 = ex2_approx(t0);
+            const float e1 = ex2_approx(t1);
+            acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
+            pk[c * 16 + (i >> 1)] = pack_half2(e0, e1);
+          }
+        float s0, s1, s2, s3;
+        f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+        f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
+        // Staging tile `buf` and the output CTA's P buffer `buf` are free
+        // once P V_{j-2} is done (that MMA read what the copy delivered).
+        if (j >= 2 && !mbar_wait_cluster_warp(&bars[PB_PFREE + buf], (uint32_t)((u - 1) & 1), ab)) {
+          ok = false;
+          break;
+        }
+        uint8_t *stg = sm + buf * 32768 + half * 16384;  // this half's 64 keys
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(smem_u32(stg) + sw128_offset((uint32_t)row, (uint32_t)ch), pk[ch * 4], pk[ch * 4 + 1],
+                       pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const uint32_t rbar = r_pfull0 + (uint32_t)(buf * 8);
+        if (lane == 0)
+          bulk_copy_to_cluster(r_base + (uint32_t)(buf * 32768 + half * 16384 + q4 * 4096), stg + q4 * 4096, 4096u,
+                               rbar);
+        if (half == 0) {
+          st_async_b32(r_alpha + (uint32_t)((buf * 128 + row) * 4), __float_as_uint(alpha), rbar);
+          if (lane == 0) st_async_b32(r_flags + (uint32_t)((buf * 4 + q4) * 4), rescale ? 1u : 0u, rbar);
+        }
+      }
+      if (ok) {
+        // Combine the two halves' row sums (exchange slot of parity n) and
+        // send them to the output CTA.
+        xch[((n & 1) * 2 + half) * 128 + row] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
+        if (mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(n & 1), ab)) {
+          l += xch[((n & 1) * 2 + (half ^ 1)) * 128 + row];
+          if (half == 0) st_async_b32(r_lsum + (uint32_t)(row * 4), __float_as_uint(l), r_lfull);
+        }
+      }
+    }
+  } else {
+    // ==================================================== output CTA ======
+    if (warp == 1) {
+      if (lane == 0) {
+        const uint64_t pd = sdesc_k128(smem_u32(sm));
+        const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING));
+        const uint32_t idesc = idesc_f16(BQ, 256);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true, issued = false;
+        for (int j = 0; j < n && ok; ++j) {
+          const int buf = j & 1, u = j >> 1;
+          if (!mbar_wait_cluster(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab) ||
+              !mbar_wait(&bars[PB_OREADY + buf], (uint32_t)(u & 1), ab)) {
+            ok = false;
+            break;
+          }
+          if (j + 2 < n) mbar_arrive_expect_tx(&bars[PB_PFULL + buf], PMSG_BYTES);
+          fence_proxy_async_smem();
+          tc_fence_after();
+          for (int r = 0; r < 4 && ok; ++r) {
+            if (!mbar_wait(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t a0 = pd + (uint64_t)(buf * 2048 + (r & 1) * 1024);
+            const uint64_t b0 = rd + (uint64_t)(s * slot16);
+            const uint32_t d_o = tmem + (uint32_t)((r >> 1) * 256);
+            const uint32_t first = (j > 0 || (r & 1) > 0) ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (first | kk) ? 1u : 0u);
+            mma_commit(&bars[PB_EMPTY + s]);
+            issued = true;
+            if (++s == PNST) { s = 0; ph ^= 1u; }
+          }
+          if (ok) mma_commit(&bars[PB_PVDONE + buf]);
+        }
+        if (ok) mma_commit(&bars[PB_OFINAL]);
+        if (!ok && issued) {
+          mma_commit(&bars[PB_DRAIN]);
+          mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
+        }
       }
       __syncwarp();
-      tmem_st32(lane_base + (uint32_t)(cb / 2), pk[0]);
-      tmem_st32(lane_base + (uint32_t)(cb / 2 + 32), pk[1]);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok) {
-      // Combine the two halves' row sums (exchange slot of parity n).
-      xch[((n & 1) * 2 + half) * 128 + row] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xbar[q4]);
-      if (!mbar_wait_warp(&xbar[q4], (uint32_t)(n & 1), ab)) ok = false;
-      else l += xch[((n & 1) * 2 + (half ^ 1)) * 128 + row];
-    }
-    if (ok && mbar_wait_warp(o_done, (n - 1) & 1, ab)) {
-      __syncwarp();
-      tc_fence_after();
-      const float inv = 1.0f / l;
-      const int b = bh / args.h, hd = bh % args.h;
-      uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
-      for (int cc = half; cc < 16; cc += 2) {
-        uint32_t t[16];
-        tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
-        tmem_wait_ld();
-        if (query >= args.N) continue;
-        const int e0 = oc * 256 + cc * 16;
-        uint4 w0, w1;
-        w0.x = pack_half2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
-        w0.y = pack_half2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
-        w0.z = pack_half2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
-        w0.w = pack_half2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
-        w1.x = pack_half2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
-        w1.y = pack_half2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
-        w1.z = pack_half2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
-        w1.w = pack_half2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
-        reinterpret_cast<uint4 *>(orow + e0)[0] = w0;
-        reinterpret_cast<uint4 *>(orow + e0)[1] = w1;
+    } else {
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const int query = q0 + row;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      bool ok = true;
+      if (warp < 6) {
+        // Rescale O rows before P_j V_j when the score CTA raised their
+        // running maximum.
+        const volatile float *alpha_s = reinterpret_cast<const volatile float *>(sm + P_ALPHA);
+        const volatile uint32_t *flags = reinterpret_cast<const volatile uint32_t *>(sm + P_FLAGS);
+        for (int j = 0; j < n; ++j) {
+          const int buf = j & 1, u = j >> 1;
+          if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
+          if (j > 0 && flags[buf * 4 + q4] != 0u) {
+            if (!mbar_wait_warp(&bars[PB_PVDONE + ((j - 1) & 1)], (uint32_t)(((j - 1) >> 1) & 1), ab)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float a = alpha_s[buf * 128 + row];
+            for (int cc = 0; cc < 32; ++cc) {
+              uint32_t t[16];
+              tmem_ld16(lane_base + (uint32_t)(cc * 16), t);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * a);
+              tmem_st16(lane_base + (uint32_t)(cc * 16), t);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[PB_OREADY + buf]);
+        }
+      } else if (warp == 6) {
+        // Hand P buffers back to the score CTA as their P V completes.
+        const uint32_t r_pfree0 = mapa_u32(smem_u32(&bars[PB_PFREE]), 0u);
+        if (lane == 0)
+          for (int j = 0; j + 2 < n; ++j) {
+            if (!mbar_wait(&bars[PB_PVDONE + (j & 1)], (uint32_t)((j >> 1) & 1), ab)) break;
+            mbar_arrive_remote(r_pfree0 + (uint32_t)((j & 1) * 8));
+          }
+        __syncwarp();
+      }
+      // Epilogue: O / l for this CTA's 128 queries, warps (q4, half) each
+      // writing 16 of the 32 16-column chunks of their rows.  (Warps 6-9 take
+      // no part in the tile loop, so they wait on the one-phase barriers.)
+      const int half = (warp - 2) >> 2;
+      if (__all_sync(0xFFFFFFFFu, ok) && mbar_wait_warp(&bars[PB_OFINAL], 0u, ab) &&
+          mbar_wait_cluster_warp(&bars[PB_LFULL], 0u, ab)) {
+        tc_fence_after();
+        const float inv = 1.0f / reinterpret_cast<const volatile float *>(sm + P_LSUM)[row];
+        const int b = bh / args.h, hd = bh % args.h;
+        uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
+        for (int cc = half; cc < 32; cc += 2) {
+          uint32_t t[16];
+          tmem_ld16(lane_base + (uint32_t)(cc * 16), t);
+          tmem_wait_ld();
+          if (query >= args.N) continue;
+          uint4 w0, w1;
+          w0.x = pack_half2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
+          w0.y = pack_half2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
+          w0.z = pack_half2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
+          w0.w = pack_half2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
+          w1.x = pack_half2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
+          w1.y = pack_half2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
+          w1.z = pack_half2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
+          w1.w = pack_half2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
+          reinterpret_cast<uint4 *>(orow + cc * 16)[0] = w0;
+          reinterpret_cast<uint4 *>(orow + cc * 16)[1] = w1;
+        }
       }
     }
   }
 
+  // ---------------------------------------------------------------- teardown
+  // Neither CTA leaves while the other may still touch its shared memory.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-int launch_attention_wide(const Dims &dm, AttnArgs a, const uint16_t *q, const uint16_t *k, const uint16_t *vt,
+int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const uint16_t *k, const uint16_t *vt,
                           cudaStream_t st) {
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int nst = (int)(((long long)max_smem - (long long)wide_smem(0)) / (WSLOT + 16));
-  if (nst > 4) nst = 4;
-  if (nst < 2) return 2;
-  a.nst = nst;
-  a.nqb = 8;
-  CUtensorMap qmap, kmap, vmap;
+  if ((int)P_SMEM > max_smem) return 2;
+  a.q = q;
+  a.ldq = dm.ldq;
+  CUtensorMap kmap, vmap;
   const uint64_t BH = (uint64_t)dm.B * dm.h;
   {
-    const uint64_t dims[3] = {(uint64_t)dm.ldq, (uint64_t)dm.N, BH};
-    const uint64_t strides[2] = {(uint64_t)dm.ldq * 2, (uint64_t)dm.N * dm.ldq * 2};
-    const uint32_t qbox[3] = {64, BQ, 1};
-    const uint32_t kbox[3] = {64, BKW, 1};
-    if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, strides, qbox,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return 1;
-    if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, strides, kbox,
+    // K viewed as [bh][64-dim chunk][key][64 dims]: one load = 2 chunks x 128 keys.
+    const uint64_t dims[4] = {64, (uint64_t)dm.N, (uint64_t)dm.ldq / 64, BH};
+    const uint64_t strides[3] = {(uint64_t)dm.ldq * 2, 128, (uint64_t)dm.N * dm.ldq * 2};
+    const uint32_t box[4] = {64, PK, 2, 1};
+    if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, k, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
@@ -778,10 +894,9 @@ int launch_attention_wide(const Dims &dm, AttnArgs a, const uint16_t *q, const u
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  const uint32_t smem = wide_smem(nst);
-  cudaFuncSetAttribute(attention_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaFuncSetAttribute(attention_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   const dim3 grid((dm.N + BQ - 1) / BQ * 2, (unsigned)BH, 1);
-  attention_wide_kernel<<<grid, 320, smem, st>>>(qmap, kmap, vmap, a);
+  attention_pair_kernel<<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
@@ -793,13 +908,13 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
   a.nqb = (dm.dp + 63) / 64;
   a.ntiles = (dm.N + BKV - 1) / BKV;
-  if (dm.dp == 512 && dm.n_oc == 2) {
+  if (dm.dp == 512) {
     a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
     a.o = o;
     a.err = kp.err;
     a.timeout_ns = kp.timeout_ns;
     a.N = dm.N; a.h = dm.h; a.d = dm.d; a.ldc = dm.ldc;
-    return launch_attention_wide(dm, a, q, k, vt, st);
+    return launch_attention_pair(dm, a, q, k, vt, st);
   }
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
