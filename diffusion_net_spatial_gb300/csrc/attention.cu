@@ -457,22 +457,31 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
 //                        the rare rescales to O before P_j V_j; at the end
 //                        O / l is written out.
 // Two producer warps per CTA issue the TMA loads (alternate ring slots): one
-// issuing thread cannot keep a ring of 32 KB boxes busy on this GPU.
+// issuing thread cannot keep a ring of 32 KB boxes busy on this GPU.  The
+// score -> output hand-off of a P tile takes about a microsecond, so the
+// output CTA keeps three P buffers, and a staging tile of the score CTA is
+// handed back as soon as its copy has landed.
 constexpr int PK = 128;          // keys per tile
 constexpr int PSLOT = 32768;     // ring slot: 32 KB of swizzled K or V^T blocks
-constexpr int PNST = 5;          // ring slots
+constexpr int PNPB = 3;          // P buffers in the output CTA
+constexpr int PNST_S = 5;        // ring slots, score CTA (after two 32 KB staging tiles)
+constexpr int PNST_O = 4;        // ring slots, output CTA (after the P buffers)
+constexpr int PNST_MAX = 5;
 constexpr int PTHREADS = 352;    // warps: 0, 10 producers; 1 MMA; 2-9 softmax / rescale + epilogue
-constexpr uint32_t P_RING = 65536;                   // after the P area (two 32 KB tiles)
-constexpr uint32_t P_SMALL = P_RING + PNST * PSLOT;  // 2 KB: xch (rank 0) | alpha, flags, lsum (rank 1)
-constexpr uint32_t P_ALPHA = P_SMALL;                // [2 buffers][128] f32
-constexpr uint32_t P_FLAGS = P_SMALL + 1024;         // [2 buffers][4 quarters] u32
-constexpr uint32_t P_LSUM = P_SMALL + 1088;          // [128] f32
-constexpr uint32_t P_BARS = P_SMALL + 2048;
+constexpr uint32_t P_RING_S = 2 * 32768;
+constexpr uint32_t P_RING_O = PNPB * 32768;
+constexpr uint32_t P_SMALL = P_RING_S + PNST_S * PSLOT;  // xch (rank 0) | alpha, flags, lsum (rank 1)
+static_assert(P_RING_O + PNST_O * PSLOT <= P_SMALL, "output CTA layout");
+constexpr uint32_t P_ALPHA = P_SMALL;                // [PNPB][128] f32
+constexpr uint32_t P_FLAGS = P_SMALL + PNPB * 512;   // [PNPB][4 quarters] u32
+constexpr uint32_t P_LSUM = P_FLAGS + PNPB * 16;     // [128] f32
+constexpr uint32_t P_BARS = P_SMALL + 2560;
+static_assert(P_LSUM + 512 <= P_BARS, "small area");
 enum {
-  PB_FULL = 0, PB_EMPTY = PB_FULL + PNST, PB_QREADY = PB_EMPTY + PNST, PB_SFULL = PB_QREADY + 1,
-  PB_SFREE = PB_SFULL + 2, PB_PFREE = PB_SFREE + 2, PB_XBAR = PB_PFREE + 2, PB_PFULL = PB_XBAR + 4,
-  PB_OREADY = PB_PFULL + 2, PB_PVDONE = PB_OREADY + 2, PB_LFULL = PB_PVDONE + 2, PB_OFINAL = PB_LFULL + 1,
-  PB_DRAIN = PB_OFINAL + 1, PB_COUNT = PB_DRAIN + 1
+  PB_FULL = 0, PB_EMPTY = PB_FULL + PNST_MAX, PB_QREADY = PB_EMPTY + PNST_MAX, PB_SFULL = PB_QREADY + 1,
+  PB_SFREE = PB_SFULL + 2, PB_STGFREE = PB_SFREE + 2, PB_PFREE = PB_STGFREE + 2, PB_XBAR = PB_PFREE + PNPB,
+  PB_PFULL = PB_XBAR + 4, PB_OREADY = PB_PFULL + PNPB, PB_PVDONE = PB_OREADY + PNPB, PB_LFULL = PB_PVDONE + PNPB,
+  PB_OFINAL = PB_LFULL + 1, PB_DRAIN = PB_OFINAL + 1, PB_COUNT = PB_DRAIN + 1
 };
 constexpr uint32_t P_SMEM = P_BARS + PB_COUNT * 8 + 16;
 constexpr uint32_t PMSG_BYTES = 32768 + 512 + 16;  // P tile + alpha + flags per key tile
@@ -500,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   const int nloads = n * 4;  // ring loads per CTA: 4 x 32 KB per key tile
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < PNST; ++i) {
+    for (int i = 0; i < PNST_MAX; ++i) {
       mbar_init(&bars[PB_FULL + i], 1);
       mbar_init(&bars[PB_EMPTY + i], 1);
     }
@@ -508,6 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[PB_SFULL + b], 1);
       mbar_init(&bars[PB_SFREE + b], 8);
+      mbar_init(&bars[PB_STGFREE + b], 1);
+    }
+    for (int b = 0; b < PNPB; ++b) {
       mbar_init(&bars[PB_PFREE + b], 1);
       mbar_init(&bars[PB_PFULL + b], 1);
       mbar_init(&bars[PB_OREADY + b], 4);
@@ -520,10 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     *abort_flag = 0u;
     fence_barrier_init();
     if (rank == 1) {
-      // Armed for the first two key tiles and for the row sums; the bytes
+      // Armed for the first PNPB key tiles and for the row sums; the bytes
       // come from the score CTA.
-      mbar_arrive_expect_tx(&bars[PB_PFULL + 0], PMSG_BYTES);
-      if (n > 1) mbar_arrive_expect_tx(&bars[PB_PFULL + 1], PMSG_BYTES);
+      for (int b = 0; b < PNPB && b < n; ++b) mbar_arrive_expect_tx(&bars[PB_PFULL + b], PMSG_BYTES);
       mbar_arrive_expect_tx(&bars[PB_LFULL], 512u);
       tma_prefetch_desc(&vmap);
     } else {
@@ -543,62 +554,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
 
   if (warp == 0 || warp == 10) {
     // ------------------------------------------------------ TMA producers
-    // Load t goes to slot t mod PNST; warp 0 issues the even loads, warp 10
+    // Load t goes to ring slot t mod nst; warp 0 issues the even loads, warp 10
     // the odd ones.  Rank 0: K as [2 x 64 dims] x 128 keys per load (4 per
     // key tile); rank 1: V^T as [256 output dims x 64 keys] (output half 0,
     // then half 1, two key blocks each).
     if (lane == 0) {
       const int me = warp == 0 ? 0 : 1;
+      const int nst = rank == 0 ? PNST_S : PNST_O;
+      uint8_t *ring = sm + (rank == 0 ? P_RING_S : P_RING_O);
       int last = -1;
       for (int t = me; t < nloads; t += 2) {
-        const int s = t % PNST, round = t / PNST;
+        const int s = t % nst, round = t / nst;
         if (round > 0 && !mbar_wait(&bars[PB_EMPTY + s], (uint32_t)((round - 1) & 1), ab)) break;
         mbar_arrive_expect_tx(&bars[PB_FULL + s], (uint32_t)PSLOT);
         const int j = t >> 2, r = t & 3;
         if (rank == 0)
-          tma_load_4d(sm + P_RING + s * PSLOT, &kmap, &bars[PB_FULL + s], 0, j * PK, 2 * r, bh);
+          tma_load_4d(ring + s * PSLOT, &kmap, &bars[PB_FULL + s], 0, j * PK, 2 * r, bh);
         else
-          tma_load_3d(sm + P_RING + s * PSLOT, &vmap, &bars[PB_FULL + s], j * PK + (r & 1) * 64, (r >> 1) * 256, bh);
+          tma_load_3d(ring + s * PSLOT, &vmap, &bars[PB_FULL + s], j * PK + (r & 1) * 64, (r >> 1) * 256, bh);
         last = t;
       }
       // After an abort no load may still be landing when the CTA leaves.
       if (*abort_flag)
-        for (int t = last; t >= 0 && t > last - 2 * PNST; t -= 2)
-          mbar_wait_drain(&bars[PB_FULL + t % PNST], (uint32_t)((t / PNST) & 1), ab.limit_ns);
+        for (int t = last; t >= 0 && t > last - 2 * nst; t -= 2)
+          mbar_wait_drain(&bars[PB_FULL + t % nst], (uint32_t)((t / nst) & 1), ab.limit_ns);
     }
     __syncwarp();
   } else if (rank == 0) {
     // ===================================================== score CTA ======
     if (warp == 1) {
-      if (lane == 0) {
-        const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING));
-        const uint32_t idesc = idesc_f16(BQ, PK);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = mbar_wait(&bars[PB_QREADY], 0, ab), issued = false;
-        for (int j = 0; j < n && ok; ++j) {
-          const int buf = j & 1, u = j >> 1;
-          if (j >= 2 && !mbar_wait(&bars[PB_SFREE + buf], (uint32_t)((u - 1) & 1), ab)) { ok = false; break; }
+      // The whole warp runs the issue loop and one elected lane issues: a
+      // loop run by a single divergent lane cannot keep N = 128 MMAs back to
+      // back.  The elected lane is always lane 0, so every commit tracks all
+      // MMAs issued before it.
+      const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING_S));
+      const uint32_t idesc = idesc_f16(BQ, PK);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = mbar_wait_warp(&bars[PB_QREADY], 0, ab), issued = false;
+      for (int j = 0; j < n && ok; ++j) {
+        const int buf = j & 1, u = j >> 1;
+        if (j >= 2 && !mbar_wait_warp(&bars[PB_SFREE + buf], (uint32_t)((u - 1) & 1), ab)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_s = tmem + (uint32_t)(buf * PK);
+        for (int c = 0; c < 4 && ok; ++c) {
+          if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_s = tmem + (uint32_t)(buf * PK);
-          for (int c = 0; c < 4 && ok; ++c) {
-            if (!mbar_wait(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t b0 = rd + (uint64_t)(s * slot16);
+          const uint64_t b0 = rd + (uint64_t)(s * slot16);
+          if (elect_one()) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // 16 dims per step; Q dims 2c' and 2c'+1 in column 256 + c'
-              mma_f16_ts(d_s, tmem + 256u + (uint32_t)((c * 8 + ks) * 8), b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
-                         idesc, (c | ks) ? 1u : 0u);
+              mma_f16_ts(d_s, tmem + 256u + (uint32_t)((c * 8 + ks) * 8),
+                         b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), idesc, (c | ks) ? 1u : 0u);
             mma_commit(&bars[PB_EMPTY + s]);
-            issued = true;
-            if (++s == PNST) { s = 0; ph ^= 1u; }
           }
-          if (ok) mma_commit(&bars[PB_SFULL + buf]);
+          __syncwarp();
+          issued = true;
+          if (++s == PNST_S) { s = 0; ph ^= 1u; }
         }
-        if (!ok && issued) {
-          mma_commit(&bars[PB_DRAIN]);
-          mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
+        if (ok) {
+          if (elect_one()) mma_commit(&bars[PB_SFULL + buf]);
+          __syncwarp();
         }
+      }
+      if (!ok && issued) {
+        if (elect_one()) mma_commit(&bars[PB_DRAIN]);
+        __syncwarp();
+        mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
       }
       __syncwarp();
     } else {
@@ -704,9 +726,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
         f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
         l = l * alpha + ((s0 + s1) + (s2 + s3));
-        // Staging tile `buf` and the output CTA's P buffer `buf` are free
-        // once P V_{j-2} is done (that MMA read what the copy delivered).
-        if (j >= 2 && !mbar_wait_cluster_warp(&bars[PB_PFREE + buf], (uint32_t)((u - 1) & 1), ab)) {
+        // Staging tile `buf` is free once the copy of tile j-2 has landed;
+        // the output CTA's P buffer `pb` once its P V_{j-PNPB} is done.
+        const int pb = j % PNPB, up = j / PNPB;
+        if (j >= 2 && !mbar_wait_cluster_warp(&bars[PB_STGFREE + buf], (uint32_t)((u - 1) & 1), ab)) {
+          ok = false;
+          break;
+        }
+        if (j >= PNPB && !mbar_wait_cluster_warp(&bars[PB_PFREE + pb], (uint32_t)((up - 1) & 1), ab)) {
           ok = false;
           break;
         }
@@ -717,13 +744,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
                        pk[ch * 4 + 2], pk[ch * 4 + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        const uint32_t rbar = r_pfull0 + (uint32_t)(buf * 8);
+        const uint32_t rbar = r_pfull0 + (uint32_t)(pb * 8);
         if (lane == 0)
-          bulk_copy_to_cluster(r_base + (uint32_t)(buf * 32768 + half * 16384 + q4 * 4096), stg + q4 * 4096, 4096u,
+          bulk_copy_to_cluster(r_base + (uint32_t)(pb * 32768 + half * 16384 + q4 * 4096), stg + q4 * 4096, 4096u,
                                rbar);
         if (half == 0) {
-          st_async_b32(r_alpha + (uint32_t)((buf * 128 + row) * 4), __float_as_uint(alpha), rbar);
-          if (lane == 0) st_async_b32(r_flags + (uint32_t)((buf * 4 + q4) * 4), rescale ? 1u : 0u, rbar);
+          st_async_b32(r_alpha + (uint32_t)((pb * 128 + row) * 4), __float_as_uint(alpha), rbar);
+          if (lane == 0) st_async_b32(r_flags + (uint32_t)((pb * 4 + q4) * 4), rescale ? 1u : 0u, rbar);
         }
       }
       if (ok) {
@@ -741,44 +768,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   } else {
     // ==================================================== output CTA ======
     if (warp == 1) {
-      if (lane == 0) {
-        const uint64_t pd = sdesc_k128(smem_u32(sm));
-        const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING));
-        const uint32_t idesc = idesc_f16(BQ, 256);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true, issued = false;
-        for (int j = 0; j < n && ok; ++j) {
-          const int buf = j & 1, u = j >> 1;
-          if (!mbar_wait_cluster(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab) ||
-              !mbar_wait(&bars[PB_OREADY + buf], (uint32_t)(u & 1), ab)) {
-            ok = false;
-            break;
-          }
-          if (j + 2 < n) mbar_arrive_expect_tx(&bars[PB_PFULL + buf], PMSG_BYTES);
-          fence_proxy_async_smem();
+      // Warp-uniform issue loop, elected lane 0 issues (as in the score CTA).
+      const uint64_t pd = sdesc_k128(smem_u32(sm));
+      const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING_O));
+      const uint32_t idesc = idesc_f16(BQ, 256);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true, issued = false;
+      for (int j = 0; j < n && ok; ++j) {
+        const int buf = j % PNPB, u = j / PNPB;
+        if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab) ||
+            !mbar_wait_warp(&bars[PB_OREADY + buf], (uint32_t)(u & 1), ab)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          if (j + PNPB < n) mbar_arrive_expect_tx(&bars[PB_PFULL + buf], PMSG_BYTES);
+          fence_proxy_async_smem();  // P and the rescale factors came from the other CTA
+        }
+        __syncwarp();
+        tc_fence_after();
+        for (int r = 0; r < 4 && ok; ++r) {
+          if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
           tc_fence_after();
-          for (int r = 0; r < 4 && ok; ++r) {
-            if (!mbar_wait(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t a0 = pd + (uint64_t)(buf * 2048 + (r & 1) * 1024);
-            const uint64_t b0 = rd + (uint64_t)(s * slot16);
-            const uint32_t d_o = tmem + (uint32_t)((r >> 1) * 256);
-            const uint32_t first = (j > 0 || (r & 1) > 0) ? 1u : 0u;
+          const uint64_t a0 = pd + (uint64_t)(buf * 2048 + (r & 1) * 1024);
+          const uint64_t b0 = rd + (uint64_t)(s * slot16);
+          const uint32_t d_o = tmem + (uint32_t)((r >> 1) * 256);
+          const uint32_t first = (j > 0 || (r & 1) > 0) ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (first | kk) ? 1u : 0u);
             mma_commit(&bars[PB_EMPTY + s]);
-            issued = true;
-            if (++s == PNST) { s = 0; ph ^= 1u; }
           }
-          if (ok) mma_commit(&bars[PB_PVDONE + buf]);
+          __syncwarp();
+          issued = true;
+          if (++s == PNST_O) { s = 0; ph ^= 1u; }
         }
-        if (ok) mma_commit(&bars[PB_OFINAL]);
-        if (!ok && issued) {
-          mma_commit(&bars[PB_DRAIN]);
-          mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
+        if (ok) {
+          if (elect_one()) mma_commit(&bars[PB_PVDONE + buf]);
+          __syncwarp();
         }
+      }
+      if (ok) {
+        if (elect_one()) mma_commit(&bars[PB_OFINAL]);
+        __syncwarp();
+      }
+      if (!ok && issued) {
+        if (elect_one()) mma_commit(&bars[PB_DRAIN]);
+        __syncwarp();
+        mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
       }
       __syncwarp();
     } else {
@@ -793,10 +832,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         const volatile float *alpha_s = reinterpret_cast<const volatile float *>(sm + P_ALPHA);
         const volatile uint32_t *flags = reinterpret_cast<const volatile uint32_t *>(sm + P_FLAGS);
         for (int j = 0; j < n; ++j) {
-          const int buf = j & 1, u = j >> 1;
+          const int buf = j % PNPB, u = j / PNPB;
           if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
           if (j > 0 && flags[buf * 4 + q4] != 0u) {
-            if (!mbar_wait_warp(&bars[PB_PVDONE + ((j - 1) & 1)], (uint32_t)(((j - 1) >> 1) & 1), ab)) {
+            if (!mbar_wait_warp(&bars[PB_PVDONE + (j - 1) % PNPB], (uint32_t)(((j - 1) / PNPB) & 1), ab)) {
               ok = false;
               break;
             }
@@ -820,9 +859,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         // Hand P buffers back to the score CTA as their P V completes.
         const uint32_t r_pfree0 = mapa_u32(smem_u32(&bars[PB_PFREE]), 0u);
         if (lane == 0)
+          for (int j = 0; j + PNPB < n; ++j) {
+            if (!mbar_wait(&bars[PB_PVDONE + j % PNPB], (uint32_t)((j / PNPB) & 1), ab)) break;
+            mbar_arrive_remote(r_pfree0 + (uint32_t)((j % PNPB) * 8));
+          }
+        __syncwarp();
+      } else if (warp == 7) {
+        // Hand staging tiles back to the score CTA as their copies land.
+        const uint32_t r_stgfree0 = mapa_u32(smem_u32(&bars[PB_STGFREE]), 0u);
+        if (lane == 0)
           for (int j = 0; j + 2 < n; ++j) {
-            if (!mbar_wait(&bars[PB_PVDONE + (j & 1)], (uint32_t)((j >> 1) & 1), ab)) break;
-            mbar_arrive_remote(r_pfree0 + (uint32_t)((j & 1) * 8));
+            if (!mbar_wait_cluster(&bars[PB_PFULL + j % PNPB], (uint32_t)((j / PNPB) & 1), ab)) break;
+            mbar_arrive_remote(r_stgfree0 + (uint32_t)((j & 1) * 8));
           }
         __syncwarp();
       }
