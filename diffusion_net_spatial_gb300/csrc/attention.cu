@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     // ------------------------------------------------------------ MMA issuer
     // Descriptors are formed once; a K step (32 B) or a 1024-B block offset
     // inside the swizzled tiles is a small add to the start-address field.
-    if (lane == 0) {
+    // The whole warp runs the loop and the elected lane 0 issues (a loop run
+    // by one divergent lane cannot issue short MMAs back to back); commits
+    // then track every MMA issued before them.
+    {
       const uint32_t idesc_s = idesc_f16(BQ, BKV);
       const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.vrows);
       const uint64_t qd = sdesc_k128(smem_u32(sm + L.q));
@@ -202,52 +205,65 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       auto issue_s = [&](int buf) {
         const uint32_t d_s = tmem + (uint32_t)(buf * BKV);
         for (int ksl = 0; ksl < nks && ok; ++ksl) {
-          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
+          if (!mbar_wait_warp(&full[s], ph, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t bd = rd + (uint64_t)(s * slot16);
           const int nblk = min(args.kpb, args.nqb - ksl * args.kpb);
-          for (int bl = 0; bl < nblk; ++bl) {
-            const int kb = ksl * args.kpb + bl;
-            const uint64_t a0 = qd + (uint64_t)(kb * 1024);
-            const uint64_t b0 = bd + (uint64_t)(bl * 1024);
-            const int kmax = min(4, ksteps - kb * 4);
+          if (elect_one()) {
+            for (int bl = 0; bl < nblk; ++bl) {
+              const int kb = ksl * args.kpb + bl;
+              const uint64_t a0 = qd + (uint64_t)(kb * 1024);
+              const uint64_t b0 = bd + (uint64_t)(bl * 1024);
+              const int kmax = min(4, ksteps - kb * 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              if (kk < kmax) mma_f16_ss(d_s, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_s, (kb | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                if (kk < kmax)
+                  mma_f16_ss(d_s, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_s, (kb | kk) ? 1u : 0u);
+            }
+            mma_commit(&empty[s]);
           }
-          mma_commit(&empty[s]);
+          __syncwarp();
           issued = true;
           advance();
         }
-        if (ok) mma_commit(&s_full[buf]);
+        if (ok) {
+          if (elect_one()) mma_commit(&s_full[buf]);
+          __syncwarp();
+        }
       };
       auto issue_pv = [&](int j) {
         const uint32_t pcol = single ? (uint32_t)args.p_col : (uint32_t)((j & 1) * BKV);
         for (int vb = 0; vb < nvb && ok; ++vb) {
-          if (!mbar_wait(&full[s], ph, ab)) { ok = false; break; }
+          if (!mbar_wait_warp(&full[s], ph, ab)) { ok = false; break; }
           tc_fence_after();
           const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
           const uint32_t d_o = tmem + TM_O + (uint32_t)(vr * args.vrows);
           const uint64_t b0 = rd + (uint64_t)(s * slot16);
           const uint32_t first = (j > 0 || vh > 0) ? 1u : 0u;
-          if (p_tmem) {
-            const uint32_t a0 = tmem + pcol + (uint32_t)(vh * 32);
+          if (elect_one()) {
+            if (p_tmem) {
+              const uint32_t a0 = tmem + pcol + (uint32_t)(vh * 32);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(d_o, a0 + (uint32_t)(kk * 8), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
-          } else {
-            const uint64_t a0 = pd + (uint64_t)(vh * 1024);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ts(d_o, a0 + (uint32_t)(kk * 8), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+            } else {
+              const uint64_t a0 = pd + (uint64_t)(vh * 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+            }
+            mma_commit(&empty[s]);
           }
-          mma_commit(&empty[s]);
+          __syncwarp();
           issued = true;
           advance();
         }
-        if (ok) mma_commit(o_done);
+        if (ok) {
+          if (elect_one()) mma_commit(o_done);
+          __syncwarp();
+        }
       };
-      if (!mbar_wait(q_full, 0, ab)) ok = false;
+      if (!mbar_wait_warp(q_full, 0, ab)) ok = false;
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -255,20 +271,21 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       for (int j = 0; j < n && ok; ++j) {
         if (single) {
           if (j + 1 < n) {
-            if (!mbar_wait(s_free, j & 1, ab)) { ok = false; break; }
+            if (!mbar_wait_warp(s_free, j & 1, ab)) { ok = false; break; }
             tc_fence_after();
             issue_s(0);
           }
         } else if (j == 0 && n > 1) {
           issue_s(1);
         }
-        if (!ok || !mbar_wait(p_full, j & 1, ab)) { ok = false; break; }
+        if (!ok || !mbar_wait_warp(p_full, j & 1, ab)) { ok = false; break; }
         tc_fence_after();
         issue_pv(j);
         if (!single && j + 2 < n) issue_s(j & 1);
       }
       if (!ok && issued) {
-        mma_commit(drain);
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
         mbar_wait_drain(drain, 0, ab.limit_ns);
       }
     }

@@ -126,26 +126,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the loop and the elected lane 0 issues.
+    {
       const uint32_t idesc = idesc_f16(BM, (uint32_t)BN);
       const uint64_t ad = sdesc_k128(smem_u32(sm + a_off));
       const uint64_t bd = sdesc_k128(smem_u32(sm + b_off));
       bool ok = true, issued = false;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % ST;
-        if (!mbar_wait(&full[s], (kb / ST) & 1, ab)) { ok = false; break; }
+        if (!mbar_wait_warp(&full[s], (kb / ST) & 1, ab)) { ok = false; break; }
         tc_fence_after();
         const uint64_t a0 = ad + (uint64_t)((s * (BM * BK * 2)) >> 4);
         const uint64_t b0 = bd + (uint64_t)((s * (BN * BK * 2)) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16_ss(tmem, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
-        mma_commit(&empty[s]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss(tmem, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        __syncwarp();
         issued = true;
       }
-      if (ok) mma_commit(acc_full);
+      if (ok) {
+        if (elect_one()) mma_commit(acc_full);
+        __syncwarp();
+      }
       if (!ok && issued) {
-        mma_commit(drain);
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
         mbar_wait_drain(drain, 0, ab.limit_ns);
       }
     }

@@ -145,28 +145,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and the elected lane 0 issues.
+    {
       const uint32_t idesc = idesc_f16(BM, (uint32_t)args.BN);
       bool issued = false, ok = true;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % ST;
-        if (!mbar_wait(&b_full[s], (kb / ST) & 1, ab) || !mbar_wait(&a_full[s], (kb / ST) & 1, ab)) {
+        if (!mbar_wait_warp(&b_full[s], (kb / ST) & 1, ab) || !mbar_wait_warp(&a_full[s], (kb / ST) & 1, ab)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sm + L.as + s * (BM * BK * 2));
         const uint32_t b_addr = smem_u32(sm + L.bs + s * (args.BN * BK * 2));
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16_ss(tmem, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
-        mma_commit(&ab_empty[s]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss(tmem, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&ab_empty[s]);
+        }
+        __syncwarp();
         issued = true;
       }
-      if (ok) mma_commit(acc_full);
+      if (ok) {
+        if (elect_one()) mma_commit(acc_full);
+        __syncwarp();
+      }
       if (!ok && issued) {
-        mma_commit(drain);
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
         mbar_wait_drain(drain, 0, ab.limit_ns);
       }
     }
