@@ -301,6 +301,332 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Resident-tile variant (C <= 512): one CTA owns a 128-pixel tile and a group
+// of BN-feature slices.  The tile's GN-applied, transposed fp16 A operand
+// (128 x C) is built once into shared memory and stays there while the CTA
+// sweeps its slices, so x is read and converted once per tile instead of once
+// per slice, and slice i's epilogue overlaps slice i+1's MMAs (two TMEM
+// accumulators).
+//   warps 0, 10  TMA producers on alternate ring loads: first the tile's x
+//                blocks [64 channels][128 pixels], then the weight tiles
+//                [BN][64] of every slice
+//   warp 1       MMA warp (warp-uniform loop, elected lane issues)
+//   warps 2..9   converters (x block -> A block), then epilogues (bias, fp16,
+//                direct stores into Q/K rows and V^T rows)
+constexpr int RNST = 3;                  // ring slots of 32 KB
+constexpr int RSLOT = 32768;
+constexpr int RTHREADS = 352;
+
+struct ResArgs {
+  int C, N, h, dp, ldq, ldn, BN, nkb, nslices, spg, xbytes;
+  const float *ga;
+  const float *gs;
+  const float *bias;
+  uint16_t *q;
+  uint16_t *k;
+  uint16_t *vt;
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+// barriers: full[RNST], empty[RNST], xfree[RNST], a_ready, acc_full[2], acc_empty[2], drain
+constexpr int RNBARS = 3 * RNST + 6;
+__host__ __device__ inline uint32_t res_ring_off(int nkb) { return (uint32_t)nkb * 16384u; }
+__host__ __device__ inline uint32_t res_slot_off(int nkb) { return res_ring_off(nkb) + RNST * RSLOT; }
+__host__ __device__ inline uint32_t res_bars_off(int nkb) { return res_slot_off(nkb) + NCONV * 256; }
+__host__ __device__ inline uint32_t res_smem(int nkb) { return res_bars_off(nkb) + RNBARS * 8 + 16; }
+
+template <int DT>
+__global__ void __launch_bounds__(RTHREADS, 1)
+    qkv_resident_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                        const ResArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw;
+  // The layout needs a 1024-byte aligned base (128B-swizzled operands) and
+  // leaves no room to realign: refuse to run otherwise.
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicOr(args.err, (uint32_t)DEV_MISALIGNED);
+    return;
+  }
+  const int nkb = args.nkb;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + res_bars_off(nkb));
+  uint64_t *full = bars;
+  uint64_t *empty = bars + RNST;
+  uint64_t *xfree = bars + 2 * RNST;
+  uint64_t *a_ready = bars + 3 * RNST;
+  uint64_t *acc_full = a_ready + 1;   // [2]
+  uint64_t *acc_empty = acc_full + 2; // [2]
+  uint64_t *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + RNBARS);
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+  uint8_t *ring = sm + res_ring_off(nkb);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x;
+  const int p0 = blockIdx.y * BM;
+  const int b = blockIdx.z;
+  const int sl0 = g * args.spg;
+  const int nsl = min(args.spg, args.nslices - sl0);  // slices of this CTA
+  const int nloads = nkb + nsl * nkb;                  // x blocks, then weight tiles
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RNST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&xfree[i], NCONV);
+    }
+    mbar_init(a_ready, NCONV);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], NCONV);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&wmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, args.err, args.timeout_ns};
+
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // Load t uses slot t mod RNST.  Before refilling a slot the producer waits
+    // for the release of the slot's previous load: by the converters (xfree)
+    // for an x block, by the MMA's commit (empty) for a weight tile.  Each
+    // barrier completes once per load of its kind in that slot, in order.
+    if (lane == 0) {
+      const int me = warp == 0 ? 0 : 1;
+      int last = -1;
+      for (int t = me; t < nloads; t += 2) {
+        const int s = t % RNST;
+        const int prev = t - RNST;
+        if (prev >= 0) {
+          bool okw;
+          if (prev < nkb) {
+            okw = mbar_wait(&xfree[s], (uint32_t)((prev / RNST) & 1), ab);
+          } else {
+            const int first_w = nkb + ((s - nkb % RNST) + RNST) % RNST;  // first weight load in slot s
+            okw = mbar_wait(&empty[s], (uint32_t)(((prev - first_w) / RNST) & 1), ab);
+          }
+          if (!okw) break;
+        }
+        if (t < nkb) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)args.xbytes);
+          tma_load_3d(ring + s * RSLOT, &xmap, &full[s], p0, t * BK, b);
+        } else {
+          const int i = (t - nkb) / nkb, kb = (t - nkb) % nkb;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(args.BN * BK * 2));
+          tma_load_2d(ring + s * RSLOT, &wmap, &full[s], kb * BK, (sl0 + i) * args.BN);
+        }
+        last = t;
+      }
+      if (*abort_flag)
+        for (int t = last; t >= 0 && t > last - 2 * RNST; t -= 2)
+          mbar_wait_drain(&full[t % RNST], (uint32_t)((t / RNST) & 1), ab.limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA warp
+    const uint32_t idesc = idesc_f16(BM, (uint32_t)args.BN);
+    const uint64_t ad = sdesc_k128(smem_u32(sm));
+    const uint64_t rd = sdesc_k128(smem_u32(ring));
+    bool ok = mbar_wait_warp(a_ready, 0, ab), issued = false;
+    int t = nkb;
+    for (int i = 0; i < nsl && ok; ++i) {
+      const int buf = i & 1;
+      if (i >= 2 && !mbar_wait_warp(&acc_empty[buf], (uint32_t)(((i >> 1) - 1) & 1), ab)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(buf * 256);
+      for (int kb = 0; kb < nkb && ok; ++kb, ++t) {
+        const int s = t % RNST;
+        if (!mbar_wait_warp(&full[s], (uint32_t)((t / RNST) & 1), ab)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss(d, ad + (uint64_t)(kb * 1024 + kk * 2), rd + (uint64_t)(s * (RSLOT >> 4) + kk * 2), idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        __syncwarp();
+        issued = true;
+      }
+      if (ok) {
+        if (elect_one()) mma_commit(&acc_full[buf]);
+        __syncwarp();
+      }
+    }
+    if (!ok && issued) {
+      if (elect_one()) mma_commit(drain);
+      __syncwarp();
+      mbar_wait_drain(drain, 0, ab.limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ converters
+    const int cw = warp - 2;                 // 0..7
+    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+    const int px = q4 * 32 + lane;           // pixel row of the A tile
+    const int hc = cw >> 2;                  // channel half of a k-block
+    float *slot = reinterpret_cast<float *>(sm + res_slot_off(nkb) + cw * 256);
+    const float *ga = args.ga + (long long)b * args.C;
+    const float *gs = args.gs + (long long)b * args.C;
+    bool ok = true;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      const int s = kb % RNST;
+      const int c = kb * BK + hc * 32 + lane;
+      const float a_c = c < args.C ? __ldg(ga + c) : 0.f;
+      const float s_c = c < args.C ? __ldg(gs + c) : 0.f;
+      if (!mbar_wait_warp(&full[s], (uint32_t)((kb / RNST) & 1), ab)) { ok = false; break; }
+      __syncwarp();
+      slot[lane] = a_c;
+      slot[32 + lane] = s_c;
+      __syncwarp();
+      const uint8_t *xs = ring + s * RSLOT;
+      const uint32_t a_tile = smem_u32(sm + kb * 16384);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ch0 = hc * 32 + j * 8;
+        float z[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float xv;
+          if (DT == 0) {
+            xv = reinterpret_cast<const float *>(xs)[(ch0 + i) * BM + px];
+          } else {
+            const unsigned short u = reinterpret_cast<const unsigned short *>(xs)[(ch0 + i) * BM + px];
+            xv = __uint_as_float(((uint32_t)u) << 16);
+          }
+          z[i] = fmaf(slot[j * 8 + i], xv, slot[32 + j * 8 + i]);
+        }
+        st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_half2(z[0], z[1]),
+                     pack_half2(z[2], z[3]), pack_half2(z[4], z[5]), pack_half2(z[6], z[7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xfree[s]);
+    }
+    if (ok) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_ready);
+    }
+    // ------------------------------------------------------------ epilogues
+    const int hdp = args.h * args.dp;
+    const int pix = p0 + px;
+    for (int i = 0; i < nsl && ok; ++i) {
+      const int buf = i & 1;
+      if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
+      tc_fence_after();
+      const int fs = (sl0 + i) * args.BN;
+      const int ncol = args.BN / 2;
+      if (args.dp % 32 == 0 && ncol % 32 == 0) {
+        // Warp (q4, hc) takes columns [hc * BN/2, (hc+1) * BN/2) of the slice,
+        // 32 at a time (never straddling a head or section when dp % 32 == 0).
+        // Q/K rows are written 64 contiguous bytes per row: a 4 x 4 shuffle
+        // transpose inside each group of 4 lanes makes lanes 4g..4g+3 write
+        // the four 16-byte pieces of one row per store instruction.
+        const int cbase = hc * ncol;
+        const int j4 = lane & 3, g4 = lane & ~3;
+        for (int c32 = 0; c32 < ncol; c32 += 32) {
+          const int f0 = fs + cbase + c32;
+          const float bl = __ldg(args.bias + f0 + lane);
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(buf * 256 + cbase + c32), r);
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) + __shfl_sync(0xFFFFFFFFu, bl, k);
+          const int sec = f0 / hdp;
+          const int hd = (f0 / args.dp) % args.h;
+          const int e0 = f0 % args.dp;
+          const long long bh = (long long)b * args.h + hd;
+          if (sec < 2) {
+            uint32_t a[4][4];  // a[k] = this row's 16-byte piece k (features 8k .. 8k+7)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              // transpose the 4 x 4 matrix (lane j of the group, piece k) -> (lane k, piece j)
+              const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
+              const uint32_t s1 = (j4 & 1) ? a[2][m] : a[3][m];
+              const uint32_t t0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+              const uint32_t t1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+              if (j4 & 1) { a[0][m] = t0; a[2][m] = t1; } else { a[1][m] = t0; a[3][m] = t1; }
+              const uint32_t u0 = (j4 & 2) ? a[0][m] : a[2][m];
+              const uint32_t u1 = (j4 & 2) ? a[1][m] : a[3][m];
+              const uint32_t w0 = __shfl_xor_sync(0xFFFFFFFFu, u0, 2);
+              const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, u1, 2);
+              if (j4 & 2) { a[0][m] = w0; a[1][m] = w1; } else { a[2][m] = w0; a[3][m] = w1; }
+            }
+            uint16_t *base = (sec == 0 ? args.q : args.k) + bh * args.N * args.ldq + e0 + j4 * 8;
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              const int rp = p0 + q4 * 32 + g4 + ii;  // row written by this group in store ii
+              if (rp < args.N)
+                *reinterpret_cast<uint4 *>(base + (long long)rp * args.ldq) = make_uint4(a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
+            }
+          } else if (pix < args.N) {
+            __half *dst = reinterpret_cast<__half *>(args.vt) + (bh * args.dp + e0) * args.ldn + pix;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) dst[(long long)k * args.ldn] = __float2half_rn(v[k]);
+          }
+        }
+      } else {
+        for (int c16 = hc; c16 < args.BN / 16; c16 += 2) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(buf * 256 + c16 * 16), r);
+          tmem_wait_ld();
+          const int f0 = fs + c16 * 16;
+          const int sec = f0 / hdp;
+          const int hd = (f0 / args.dp) % args.h;
+          const int e0 = f0 % args.dp;
+          const long long bh = (long long)b * args.h + hd;
+          float v[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]) + __ldg(args.bias + f0 + k);
+          if (pix >= args.N) continue;
+          if (sec < 2) {
+            uint16_t *dst = (sec == 0 ? args.q : args.k) + (bh * args.N + pix) * args.ldq + e0;
+            uint4 w0, w1;
+            w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
+            w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
+            w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
+            w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
+            reinterpret_cast<uint4 *>(dst)[0] = w0;
+            reinterpret_cast<uint4 *>(dst)[1] = w1;
+          } else {
+            __half *dst = reinterpret_cast<__half *>(args.vt) + (bh * args.dp + e0) * args.ldn + pix;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) dst[(long long)k * args.ldn] = __float2half_rn(v[k]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 int pick_bn(int ntot) {
   for (int bn = 256; bn >= 16; bn -= 16)
     if (ntot % bn == 0) return bn;
@@ -349,6 +675,36 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     if (encode_tiled(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, vdims, vstrides, vbox,
                      CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return 1;
+  }
+  const int nkb = (dm.C + BK - 1) / BK;
+  int max_smem = 232448, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (BN <= 256 && BN * BK * 2 <= RSLOT && BM * BK * es <= RSLOT && (int)res_smem(nkb) <= max_smem) {
+    int nsm = 148;
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int mtiles = dm.B * ((dm.N + BM - 1) / BM);
+    const int nslices = dm.ntot / BN;
+    int ng = nsm / mtiles;
+    if (ng < 1) ng = 1;
+    if (ng > nslices) ng = nslices;
+    const int spg = (nslices + ng - 1) / ng;
+    ng = (nslices + spg - 1) / spg;
+    ResArgs r{};
+    r.C = dm.C; r.N = dm.N; r.h = dm.h; r.dp = dm.dp; r.ldq = dm.ldq; r.ldn = dm.ldn; r.BN = BN;
+    r.nkb = nkb; r.nslices = nslices; r.spg = spg; r.xbytes = BM * BK * es;
+    r.ga = ga; r.gs = gs; r.bias = b_qkv; r.q = q; r.k = k; r.vt = vt;
+    r.err = kp.err; r.timeout_ns = kp.timeout_ns;
+    const uint32_t smem = res_smem(nkb);
+    const dim3 grid(ng, (dm.N + BM - 1) / BM, dm.B);
+    if (dtype == 0) {
+      cudaFuncSetAttribute(qkv_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      qkv_resident_kernel<0><<<grid, RTHREADS, smem, st>>>(xmap, wmap, r);
+    } else {
+      cudaFuncSetAttribute(qkv_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      qkv_resident_kernel<1><<<grid, RTHREADS, smem, st>>>(xmap, wmap, r);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
   QkvArgs a{};
   a.C = dm.C; a.N = dm.N; a.h = dm.h; a.dp = dm.dp; a.ldq = dm.ldq; a.ldn = dm.ldn; a.BN = BN;
