@@ -248,6 +248,221 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Resident variant (C <= 512, TMA-addressable x/out): one CTA owns 128 pixels
+// and ALL output channels -- the O tile (128 x C fp16) is loaded once and
+// stays in shared memory, Wo streams through a ring, and the whole 128 x C
+// accumulator lives in tensor memory (C <= 512 columns).  After the MMAs the
+// freed shared memory holds two residual pieces [128 channels][128 pixels] at
+// a time: TMA loads x, eight warps add the accumulator and bias in place, TMA
+// stores out (out may alias x: each piece is read before it is written and
+// no CTA touches another CTA's pixels).
+//   warps 0, 10  TMA producers (O tile and Wo tiles; warp 0 also runs the
+//                residual pieces' loads and stores)
+//   warp 1       MMA warp (warp-uniform loop, elected lane issues)
+//   warps 2..9   epilogue
+constexpr int ORNST = 3;
+constexpr int ORSLOT = 32768;
+constexpr int ORTHREADS = 352;
+
+struct OutResArgs {
+  int C, N, nkb, nch, BNc, npieces, es;
+  const float *bias;
+  uint32_t *err;
+  uint64_t timeout_ns;
+};
+// a_full, full[ORNST], empty[ORNST], acc_full, xfull[2], piece_done[2], drain
+constexpr int ORNBARS = 2 * ORNST + 7;
+__host__ __device__ inline uint32_t ores_ring_off(int nkb) { return (uint32_t)nkb * 16384u; }
+__host__ __device__ inline uint32_t ores_bars_off(int nkb) { return ores_ring_off(nkb) + ORNST * ORSLOT; }
+__host__ __device__ inline uint32_t ores_smem(int nkb) { return ores_bars_off(nkb) + ORNBARS * 8 + 16; }
+
+template <int DT>
+__global__ void __launch_bounds__(ORTHREADS, 1)
+    out_proj_resident_kernel(const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap wmap,
+                             const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap outmap,
+                             const OutResArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw;
+  // The layout needs a 1024-byte aligned base (128B-swizzled operands) and
+  // leaves no room to realign: refuse to run otherwise.
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicOr(args.err, (uint32_t)DEV_MISALIGNED);
+    return;
+  }
+  const int nkb = args.nkb, nch = args.nch, BNc = args.BNc;
+  uint8_t *ring = sm + ores_ring_off(nkb);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + ores_bars_off(nkb));
+  uint64_t *a_full = bars;
+  uint64_t *full = bars + 1;
+  uint64_t *empty = full + ORNST;
+  uint64_t *acc_full = empty + ORNST;
+  uint64_t *xfull = acc_full + 1;       // [2]
+  uint64_t *piece_done = xfull + 2;     // [2]
+  uint64_t *drain = piece_done + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + ORNBARS);
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+  const uint32_t piece_bytes = (uint32_t)(128 * 128 * args.es);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p0 = blockIdx.x * BM;
+  const int b = blockIdx.y;
+  const int nloads = nkb * nch;
+
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    for (int i = 0; i < ORNST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&piece_done[i], NEPI);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    tma_prefetch_desc(&omap);
+    tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&outmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, args.err, args.timeout_ns};
+
+  if (warp == 0 || warp == 10) {
+    if (lane == 0) {
+      const int me = warp == 0 ? 0 : 1;
+      bool ok = true;
+      if (me == 0) {
+        mbar_arrive_expect_tx(a_full, (uint32_t)(nkb * 16384));
+        for (int kb = 0; kb < nkb; ++kb) tma_load_3d(sm + kb * 16384, &omap, a_full, kb * BK, p0, b);
+      } else {
+        // Pull this tile's residual into L2 while the MMAs run.
+        for (int k = 0; k < args.npieces; ++k) tma_prefetch_3d(&xmap, p0, k * 128, b);
+      }
+      int last = -1;
+      for (int t = me; t < nloads; t += 2) {
+        const int s = t % ORNST;
+        if (t >= ORNST && !mbar_wait(&empty[s], (uint32_t)(((t / ORNST) - 1) & 1), ab)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(BNc * BK * 2));
+        tma_load_2d(ring + s * ORSLOT, &wmap, &full[s], (t / nch) * BK, (t % nch) * BNc);
+        last = t;
+      }
+      if (*abort_flag) {
+        for (int t = last; t >= 0 && t > last - 2 * ORNST; t -= 2)
+          mbar_wait_drain(&full[t % ORNST], (uint32_t)((t / ORNST) & 1), ab.limit_ns);
+        if (me == 0) mbar_wait_drain(a_full, 0, ab.limit_ns);
+      }
+      if (me == 0 && ok && !*abort_flag) {
+        // Residual pieces, once every MMA (the last readers of the shared
+        // memory they reuse) has completed.
+        if (mbar_wait(acc_full, 0, ab)) {
+          for (int k = 0; k < 2 && k < args.npieces; ++k) {
+            mbar_arrive_expect_tx(&xfull[k], piece_bytes);
+            tma_load_3d(sm + k * piece_bytes, &xmap, &xfull[k], p0, k * 128, b);
+          }
+          for (int k = 0; k < args.npieces; ++k) {
+            const int bf = k & 1;
+            if (!mbar_wait(&piece_done[bf], (uint32_t)((k >> 1) & 1), ab)) break;
+            tma_store_3d(&outmap, sm + bf * piece_bytes, p0, k * 128, b);
+            tma_store_commit();
+            if (k + 2 < args.npieces) {
+              tma_store_wait_read();  // the buffer's store has read it
+              mbar_arrive_expect_tx(&xfull[bf], piece_bytes);
+              tma_load_3d(sm + bf * piece_bytes, &xmap, &xfull[bf], p0, (k + 2) * 128, b);
+            }
+          }
+          tma_store_wait_all();
+        }
+        if (*abort_flag)
+          for (int k = 0; k < 2 && k < args.npieces; ++k) mbar_wait_drain(&xfull[k], 0, ab.limit_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    const uint32_t idesc = idesc_f16(BM, (uint32_t)BNc);
+    const uint64_t ad = sdesc_k128(smem_u32(sm));
+    const uint64_t rd = sdesc_k128(smem_u32(ring));
+    bool ok = mbar_wait_warp(a_full, 0, ab), issued = false;
+    for (int t = 0; t < nloads && ok; ++t) {
+      const int s = t % ORNST, kb = t / nch, c = t % nch;
+      if (!mbar_wait_warp(&full[s], (uint32_t)((t / ORNST) & 1), ab)) { ok = false; break; }
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_f16_ss(tmem + (uint32_t)(c * BNc), ad + (uint64_t)(kb * 1024 + kk * 2),
+                     rd + (uint64_t)(s * (ORSLOT >> 4) + kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+      issued = true;
+    }
+    if (ok) {
+      if (elect_one()) mma_commit(acc_full);
+      __syncwarp();
+    }
+    if (!ok && issued) {
+      if (elect_one()) mma_commit(drain);
+      __syncwarp();
+      mbar_wait_drain(drain, 0, ab.limit_ns);
+    }
+    __syncwarp();
+  } else {
+    const int ew = warp - 2;
+    const int q4 = warp & 3;
+    const int half = ew >> 2;
+    const int row = q4 * 32 + lane;
+    bool ok = mbar_wait_warp(acc_full, 0, ab);
+    for (int k = 0; k < args.npieces && ok; ++k) {
+      const int bf = k & 1;
+      if (!mbar_wait_warp(&xfull[bf], (uint32_t)((k >> 1) & 1), ab)) { ok = false; break; }
+      tc_fence_after();
+      uint8_t *xs = sm + bf * piece_bytes;
+      for (int c32 = 0; c32 < 64; c32 += 32) {
+        const int cl0 = half * 64 + c32;   // channel within the piece
+        const int c0 = k * 128 + cl0;      // output channel
+        if (c0 >= args.C) break;
+        const float bl = c0 + lane < args.C ? __ldg(args.bias + c0 + lane) : 0.f;
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float y = __uint_as_float(r[i]) + __shfl_sync(0xFFFFFFFFu, bl, i);
+          if (DT == 0) {
+            float *px = reinterpret_cast<float *>(xs) + (cl0 + i) * BM + row;
+            *px = *px + y;
+          } else {
+            __nv_bfloat16 *px = reinterpret_cast<__nv_bfloat16 *>(xs) + (cl0 + i) * BM + row;
+            *px = __float2bfloat16_rn(__bfloat162float(*px) + y);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&piece_done[bf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 int pick_bn(int C, int cap) {
   const int c16 = (C + 15) / 16 * 16;
   for (int bn = cap; bn >= 16; bn -= 16)
@@ -292,6 +507,49 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
   } else {
     xmap = omap;  // unused
     outmap = omap;
+  }
+  const int nkb = (dm.C + BK - 1) / BK;
+  int max_smem = 232448, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const int c16 = (dm.C + 15) / 16 * 16;
+  // The resident form pays off when there are enough pixel tiles to fill the
+  // GPU with one CTA each.
+  const int mtiles = dm.B * ((dm.N + BM - 1) / BM);
+  if (tma_epi && c16 <= 512 && mtiles >= 64 && (int)ores_smem(nkb) <= max_smem &&
+      2u * 128u * 128u * (uint32_t)es <= ores_bars_off(nkb)) {
+    const int nch = (c16 + 255) / 256;
+    const int BNc = ((c16 / nch + 15) / 16) * 16;
+    CUtensorMap wres, xres, outres;
+    {
+      const uint64_t dims[2] = {(uint64_t)dm.C, (uint64_t)dm.C};
+      const uint64_t strides[1] = {(uint64_t)dm.ldc * 2};
+      const uint32_t box[2] = {BK, (uint32_t)BNc};
+      if (encode_tiled(&wres, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w_o, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return 1;
+    }
+    {
+      const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.C, (uint64_t)dm.B};
+      const uint64_t strides[2] = {(uint64_t)dm.N * es, (uint64_t)dm.C * dm.N * es};
+      const uint32_t box[3] = {BM, 128, 1};
+      const CUtensorMapDataType dt = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      if (encode_tiled(&xres, dt, 3, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS) return 1;
+      if (encode_tiled(&outres, dt, 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS) return 1;
+    }
+    OutResArgs r{};
+    r.C = dm.C; r.N = dm.N; r.nkb = nkb; r.nch = nch; r.BNc = BNc; r.npieces = (dm.C + 127) / 128; r.es = es;
+    r.bias = b_o; r.err = kp.err; r.timeout_ns = kp.timeout_ns;
+    const uint32_t smem = ores_smem(nkb);
+    const dim3 grid((dm.N + BM - 1) / BM, dm.B, 1);
+    if (dtype == 0) {
+      cudaFuncSetAttribute(out_proj_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      out_proj_resident_kernel<0><<<grid, ORTHREADS, smem, st>>>(omap, wres, xres, outres, r);
+    } else {
+      cudaFuncSetAttribute(out_proj_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      out_proj_resident_kernel<1><<<grid, ORTHREADS, smem, st>>>(omap, wres, xres, outres, r);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
   OutArgs a{};
   a.C = dm.C; a.N = dm.N; a.BN = BN; a.nk = (dm.C + BK - 1) / BK;

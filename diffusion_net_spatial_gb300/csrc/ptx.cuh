@@ -191,6 +191,13 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// Prefetch a tensor tile into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // this CTA's shared memory to another CTA's; the bytes complete that CTA's
 // barrier `rbar`.
