@@ -64,6 +64,15 @@ def _load():
         [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ip, ctypes.c_int] + [dp] * 9
     )
     lib.ssa_oracle_forward.restype = ctypes.c_int
+    lib.ssa_oracle_forward_ex.argtypes = (
+        [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ctypes.c_int, ctypes.c_int, dp] + [ip, ctypes.c_int] + [dp] * 9
+    )
+    lib.ssa_oracle_forward_ex.restype = ctypes.c_int
+    lib.ssa_oracle_attention_ex.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [ip, ctypes.c_int, dp,
+                                                                                ctypes.c_int, ctypes.c_int, dp, dp]
+    lib.ssa_oracle_attention_ex.restype = None
+    lib.ssa_oracle_rope.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ip]
+    lib.ssa_oracle_rope.restype = None
     lib.ssa_oracle_attention.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [dp, dp]
     lib.ssa_oracle_attention.restype = None
     lib.ssa_oracle_out_proj.argtypes = [dp, dp, dp] + [ctypes.c_int] * 3 + [dp]
@@ -130,19 +139,31 @@ def gn_stats(x, num_groups: int):
     return mean, rstd
 
 
-def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()):
+def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=(), causal=False, rope=False,
+            rel_table=None):
     """Run the block in fp64.
 
-    x: (B, C, H, W); params: the 10 tensors keyed as on the page.
+    x: (B, C, H, W); params: the 10 tensors keyed as on the page (a bias that
+    is None or absent means that projection has no bias).
     qidx: None (every pixel) or a 1-D array of pixel indices (row i*W + j)
-    shared by every sample.  Returns a dict with 'y' (B, C, nq) = the branch
-    image([O] Wo^T + bo) at those pixels, and any of 'mean', 'rstd', 'z', 'q',
-    'k', 'v', 'o', 'p' named in ``want``.
+    shared by every sample.  causal / rope / rel_table ((2H-1)(2W-1), heads)
+    select the attention variants of the HNDL attention operator page.
+    Returns a dict with 'y' (B, C, nq) = the branch image([O] Wo^T + bo) at
+    those pixels, and any of 'mean', 'rstd', 'z', 'q', 'k', 'v', 'o', 'p'
+    named in ``want`` ('q', 'k' after the rotary embedding when rope).
     """
     x = _f64(x)
     B, C, H, W = x.shape
     N = H * W
-    p = {k: _f64(params[k]) for k in PARAM_KEYS}
+    p = {k: (None if params.get(k) is None else _f64(params[k])) for k in PARAM_KEYS}
+    for k in ("norm_weight", "norm_bias", "q_weight", "k_weight", "v_weight", "out_weight"):
+        if p[k] is None:
+            raise ValueError(f"{k} is required")
+    rel = None
+    if rel_table is not None:
+        rel = _f64(rel_table)
+        if rel.shape != ((2 * H - 1) * (2 * W - 1), num_heads):
+            raise ValueError("rel_table must be ((2H-1)(2W-1), heads)")
     G, nh = num_groups, num_heads
     if qidx is not None:
         qi = np.ascontiguousarray(np.asarray(qidx, dtype=np.int32))
@@ -155,9 +176,10 @@ def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()
               "k": (B, N, C), "v": (B, N, C), "o": (B, nq, C), "p": (B, nh, nq, N)}
     for k in want:
         out[k] = np.empty(shapes[k])
-    rc = _load().ssa_oracle_forward(
+    rc = _load().ssa_oracle_forward_ex(
         _dptr(x), B, C, H, W, G, nh,
         *[_dptr(p[k]) for k in PARAM_KEYS],
+        int(bool(causal)), int(bool(rope)), _dptr(rel),
         qptr, nq,
         _dptr(out["y"]), *[_dptr(out.get(k)) for k in ("mean", "rstd", "z", "q", "k", "v", "o", "p")])
     if rc != 0:
@@ -179,9 +201,48 @@ def attention(q, k, v, num_heads: int):
     return o
 
 
+def attention_ex(q, k, v, num_heads: int, qpos=None, causal=False, rel_table=None, H=None, W=None):
+    """The attention step with the variants: qpos (nq,) token positions of the
+    query rows (None: row t is position t), causal mask, relative-position
+    table ((2H-1)(2W-1), heads) over an H x W grid (H * W == N)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, nq, C = q.shape
+    N = k.shape[1]
+    if C % num_heads:
+        raise ValueError("num_heads must divide C")
+    qp = None
+    if qpos is not None:
+        qp = np.ascontiguousarray(np.asarray(qpos, dtype=np.int32))
+    rel = None if rel_table is None else _f64(rel_table)
+    if rel is not None and (H is None or W is None or H * W != N):
+        raise ValueError("rel_table needs H, W with H * W == N")
+    o = np.empty((B, nq, C))
+    _load().ssa_oracle_attention_ex(_dptr(q), _dptr(k), _dptr(v), B, N, nq, C, num_heads,
+                                    None if qp is None else qp.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                    int(bool(causal)), _dptr(rel), int(H or 1), int(W or 1), _dptr(o), None)
+    return o
+
+
+def rope(m, num_heads: int, pos=None):
+    """Rotary embedding (rotate-half, base 10000) of rows (..., tokens, C) by
+    token position (pos, broadcast over the leading axes; by default the
+    index along the token axis), in fp64; returns a new array."""
+    m = _f64(m).copy()
+    C = m.shape[-1]
+    rows = int(np.prod(m.shape[:-1]))
+    if C % num_heads or (C // num_heads) % 2:
+        raise ValueError("rope needs an even head dim")
+    if pos is None:
+        pos = np.arange(m.shape[-2])
+    pp = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.int32), m.shape[:-1]).reshape(-1))
+    _load().ssa_oracle_rope(_dptr(m), rows, C, num_heads, pp.ctypes.data_as(ctypes.POINTER(ctypes.c_int)))
+    return m
+
+
 def out_proj(o, out_weight, out_bias):
     """The output projection alone, in fp64: y (B, C, nq) = image(O Wo^T + bo)."""
-    o, w, b = _f64(o), _f64(out_weight), _f64(out_bias)
+    o, w = _f64(o), _f64(out_weight)
+    b = None if out_bias is None else _f64(out_bias)
     B, nq, C = o.shape
     y = np.empty((B, C, nq))
     _load().ssa_oracle_out_proj(_dptr(o), _dptr(w), _dptr(b), B, nq, C, _dptr(y))
@@ -210,14 +271,15 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u32.view(np.float32).astype(np.float64)
 
 
-def block(x, params: dict, num_groups: int, num_heads: int, qidx=None):
+def block(x, params: dict, num_groups: int, num_heads: int, qidx=None, causal=False, rope=False,
+          rel_table=None):
     """The full block with the page's dtype rule: returns (out_f64, y_f64)
     where out_f64 is x + y rounded once to x's dtype and widened back to fp64
     for comparison.  x's dtype is read from a torch tensor ('bf16' when
     torch.bfloat16) or taken as fp32 for anything else."""
     dt = "bf16" if (hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16") else "f32"
     xf = _f64(x)
-    r = forward(xf, params, num_groups, num_heads, qidx=qidx)
+    r = forward(xf, params, num_groups, num_heads, qidx=qidx, causal=causal, rope=rope, rel_table=rel_table)
     y = r["y"]
     B, C = xf.shape[:2]
     xs = xf.reshape(B, C, -1)

@@ -36,6 +36,21 @@
  * Query-sampled mode: when qidx != NULL only the nq listed pixels of every
  * sample get Q, O and the branch output; Z, K and V are still formed for all
  * H*W pixels, because every query attends to every key.
+ *
+ * Variants (HNDL "attention" operator page, parameter table and its Biases,
+ * Masking, Relative position bias and Rotary embeddings paragraphs), applied
+ * to the block's token sequence (T = H*W tokens in row-major pixel order):
+ *   * bias flags: a NULL bq / bk / bv / bo means that projection has no bias;
+ *   * causal: key m is masked (score -inf) for query position t when m > t;
+ *   * rope: Q and K rows are rotated by their token position t per head with
+ *     the rotate-half convention over the full head dim, base 10000:
+ *     theta_i = 10000^(-2i/d), angle = t * theta_i (i < d/2),
+ *     x' = x * cos(angle) + rotate_half(x) * sin(angle), rotate_half([a, b])
+ *     = [-b, a]; the rotation is evaluated exactly in fp64 here;
+ *   * relative position bias: a table [(2H-1)(2W-1)][heads]; for query token
+ *     (rq, cq) and key token (rk, ck) of the row-major grid, head j adds
+ *     table[((rq - rk + H - 1) * (2W - 1) + (cq - ck + W - 1)) * heads + j]
+ *     to the scaled logit before the softmax.
  */
 #include <math.h>
 #include <stdint.h>
@@ -76,8 +91,9 @@ int ssa_oracle_gn_stats(const double *x, int B, int C, int N, int G,
  * p (optional) [B][h][nq][N].  Per head j: scores over all keys scaled by
  * 1/sqrt(d), a softmax over the key axis (the maximum is subtracted only to
  * keep exp() in range), then P V; head outputs side by side in head order. */
-void ssa_oracle_attention(const double *q, const double *k, const double *v, int B, int N, int nq, int C,
-                          int nh, double *o, double *p_out)
+static void attention_core(const double *q, const double *k, const double *v, int B, int N, int nq, int C,
+                           int nh, const int *qpos, int causal, const double *rel, int H, int W,
+                           double *o, double *p_out)
 {
     const int d = C / nh;
     const double scale = 1.0 / sqrt((double)d);
@@ -89,6 +105,7 @@ void ssa_oracle_attention(const double *q, const double *k, const double *v, int
             for (int t = 0; t < nq; ++t) {
                 const double *qr = q + ((long long)b * nq + t) * C;
                 double *orow = o + ((long long)b * nq + t) * C;
+                const int tq = qpos ? qpos[t] : t; /* token position of this query */
                 for (int j = 0; j < nh; ++j) {
                     const int c0 = j * d;
                     double smax = -INFINITY;
@@ -97,6 +114,12 @@ void ssa_oracle_attention(const double *q, const double *k, const double *v, int
                         double acc = 0.0;
                         for (int e = 0; e < d; ++e) acc += qr[c0 + e] * kr[c0 + e];
                         s[m] = acc * scale;
+                        if (rel) {
+                            const int dy = tq / W - m / W + (H - 1);
+                            const int dx = tq % W - m % W + (W - 1);
+                            s[m] += rel[((long long)dy * (2 * W - 1) + dx) * nh + j];
+                        }
+                        if (causal && m > tq) s[m] = -INFINITY;
                         if (s[m] > smax) smax = s[m];
                     }
                     double den = 0.0;
@@ -121,6 +144,43 @@ void ssa_oracle_attention(const double *q, const double *k, const double *v, int
     }
 }
 
+void ssa_oracle_attention(const double *q, const double *k, const double *v, int B, int N, int nq, int C,
+                          int nh, double *o, double *p_out)
+{
+    attention_core(q, k, v, B, N, nq, C, nh, NULL, 0, NULL, 1, 1, o, p_out);
+}
+
+/* Attention with the variants: qpos [nq] token position of each query row
+ * (NULL: row t is position t), causal mask, relative-position table (NULL:
+ * none) over an H x W grid with H * W == N. */
+void ssa_oracle_attention_ex(const double *q, const double *k, const double *v, int B, int N, int nq, int C,
+                             int nh, const int *qpos, int causal, const double *rel, int H, int W,
+                             double *o, double *p_out)
+{
+    attention_core(q, k, v, B, N, nq, C, nh, qpos, causal, rel, H, W, o, p_out);
+}
+
+/* ---- Rotary embedding of one (rows x C) matrix, in place ------------------
+ * Row r sits at token position pos[r] (or r when pos is NULL); each head's
+ * d features are rotated pairwise (i, i + d/2) by angle pos * 10000^(-2i/d). */
+void ssa_oracle_rope(double *m, int rows, int C, int nh, const int *pos)
+{
+    const int d = C / nh, hd = d / 2;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        const double t = (double)(pos ? pos[r] : r);
+        double *row = m + (long long)r * C;
+        for (int j = 0; j < nh; ++j)
+            for (int i = 0; i < hd; ++i) {
+                const double theta = pow(10000.0, -2.0 * (double)i / (double)d);
+                const double a = row[j * d + i], bb = row[j * d + hd + i];
+                const double cs = cos(t * theta), sn = sin(t * theta);
+                row[j * d + i] = a * cs - bb * sn;       /* a cos + (-b) sin */
+                row[j * d + hd + i] = bb * cs + a * sn;  /* b cos + a sin */
+            }
+    }
+}
+
 /* ---- Step 4: output projection and image() --------------------------------
  * o [B][nq][C] -> y [B][C][nq] = (o Wo^T + bo) with the pixel axis last. */
 void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, int B, int nq, int C, double *y)
@@ -132,7 +192,7 @@ void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, in
             for (int c = 0; c < C; ++c) {
                 double acc = 0.0;
                 for (int e = 0; e < C; ++e) acc += orow[e] * wo[(long long)c * C + e];
-                y[((long long)b * C + c) * nq + t] = acc + bo[c];
+                y[((long long)b * C + c) * nq + t] = acc + (bo ? bo[c] : 0.0);
             }
         }
 }
@@ -150,20 +210,26 @@ void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, in
  *   q    [B][nq][C]  k, v [B][N][C]
  *   o    [B][nq][C]  concatenated head outputs
  *   p    [B][h][nq][N] softmax probabilities (only for small problems)
- * Returns 0; -1 on a bad shape (C % G, C % h, non-positive sizes). */
-int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int nh,
-                       const double *gw, const double *gb,
-                       const double *wq, const double *bq,
-                       const double *wk, const double *bk,
-                       const double *wv, const double *bv,
-                       const double *wo, const double *bo,
-                       const int *qidx, int nq,
-                       double *y, double *mean_out, double *rstd_out,
-                       double *z_out, double *q_out, double *k_out,
-                       double *v_out, double *o_out, double *p_out)
+ * ssa_oracle_forward_ex also takes causal, rope (both 0/1) and rel (NULL or
+ * the table [(2H-1)(2W-1)][h]); any bias pointer may be NULL (no bias); q and
+ * k are returned after the rotation when rope is set.
+ * Returns 0; -1 on a bad shape (C % G, C % h, non-positive sizes, an odd head
+ * dim with rope). */
+int ssa_oracle_forward_ex(const double *x, int B, int C, int H, int W, int G, int nh,
+                          const double *gw, const double *gb,
+                          const double *wq, const double *bq,
+                          const double *wk, const double *bk,
+                          const double *wv, const double *bv,
+                          const double *wo, const double *bo,
+                          int causal, int rope, const double *rel,
+                          const int *qidx, int nq,
+                          double *y, double *mean_out, double *rstd_out,
+                          double *z_out, double *q_out, double *k_out,
+                          double *v_out, double *o_out, double *p_out)
 {
     if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || G <= 0 || nh <= 0) return -1;
     if (C % G || C % nh) return -1;
+    if (rope && (C / nh) % 2) return -1; /* rotate-half needs an even head dim */
     const int N = H * W;
     if (!qidx) nq = N;
     if (nq <= 0) return -1;
@@ -206,8 +272,8 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
                     sk += zr[c] * wk[(long long)f * C + c];
                     sv += zr[c] * wv[(long long)f * C + c];
                 }
-                kr[f] = sk + bk[f];
-                vr[f] = sv + bv[f];
+                kr[f] = sk + (bk ? bk[f] : 0.0);
+                vr[f] = sv + (bv ? bv[f] : 0.0);
             }
         }
 #pragma omp parallel for collapse(2) schedule(static)
@@ -219,12 +285,19 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
             for (int f = 0; f < C; ++f) {
                 double s = 0.0;
                 for (int c = 0; c < C; ++c) s += zr[c] * wq[(long long)f * C + c];
-                qr[f] = s + bq[f];
+                qr[f] = s + (bq ? bq[f] : 0.0);
             }
         }
 
+    /* 2b. Rotary embedding of Q and K by token position. */
+    if (rope)
+        for (int b = 0; b < B; ++b) {
+            ssa_oracle_rope(q + (long long)b * nq * C, nq, C, nh, qidx);
+            ssa_oracle_rope(k + (long long)b * N * C, N, C, nh, NULL);
+        }
+
     /* 3. Attention per head, then 4. the output projection and image(). */
-    ssa_oracle_attention(q, k, v, B, N, nq, C, nh, o, p_out);
+    attention_core(q, k, v, B, N, nq, C, nh, qidx, causal, rel, H, W, o, p_out);
     ssa_oracle_out_proj(o, wo, bo, B, nq, C, y);
 
     if (mean_out) memcpy(mean_out, mean, sizeof(double) * B * G);
@@ -236,6 +309,21 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
     if (o_out) memcpy(o_out, o, sizeof(double) * (size_t)B * nq * C);
     free(mean); free(rstd); free(z); free(k); free(v); free(q); free(o);
     return 0;
+}
+
+int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int nh,
+                       const double *gw, const double *gb,
+                       const double *wq, const double *bq,
+                       const double *wk, const double *bk,
+                       const double *wv, const double *bv,
+                       const double *wo, const double *bo,
+                       const int *qidx, int nq,
+                       double *y, double *mean_out, double *rstd_out,
+                       double *z_out, double *q_out, double *k_out,
+                       double *v_out, double *o_out, double *p_out)
+{
+    return ssa_oracle_forward_ex(x, B, C, H, W, G, nh, gw, gb, wq, bq, wk, bk, wv, bv, wo, bo, 0, 0, NULL, qidx,
+                                 nq, y, mean_out, rstd_out, z_out, q_out, k_out, v_out, o_out, p_out);
 }
 
 /* ---- Rounding to the dtype of x -------------------------------------------
