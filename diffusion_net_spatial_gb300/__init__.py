@@ -28,7 +28,14 @@ EXPORTS = ("ssa_workspace_size", "ssa_forward", "ssa_plan_create", "ssa_plan_wor
            "ssa_forward_planned", "ssa_plan_destroy", "ssa_gn_stats", "ssa_pack_weights",
            "ssa_qkv_project", "ssa_attention", "ssa_out_project", "ssa_get_device_status",
            "ssa_set_wait_timeout_ns", "ssa_debug_timeout_probe", "ssa_last_error_string",
-           "ssa_launches_per_forward")
+           "ssa_launches_per_forward", "ssa_workspace_size_ex", "ssa_forward_ex", "ssa_plan_workspace_size_ex",
+           "ssa_forward_planned_ex", "ssa_rope", "ssa_pack_rel_table", "ssa_attention_ex")
+BIAS_KEYS = ("q_bias", "k_bias", "v_bias", "out_bias")
+
+
+class SsaOptions(ctypes.Structure):
+    """struct ssa_options of include/ssa.h (attention variants)."""
+    _fields_ = [("causal", ctypes.c_int), ("rope", ctypes.c_int), ("rel_pos_table", ctypes.c_void_p)]
 
 
 class SsaError(RuntimeError):
@@ -66,6 +73,13 @@ def load_library():
         "ssa_debug_timeout_probe": ([u64, vp], i32),
         "ssa_last_error_string": ([], ctypes.c_char_p),
         "ssa_launches_per_forward": ([i32], i32),
+        "ssa_workspace_size_ex": ([i32] * 7 + [vp], sz),
+        "ssa_forward_ex": ([vp] + [i32] * 6 + [vp] * 10 + [vp, i32, vp, vp, sz, vp], i32),
+        "ssa_plan_workspace_size_ex": ([vp, i32, i32, i32, vp], sz),
+        "ssa_forward_planned_ex": ([vp, vp, i32, i32, i32, vp, vp, vp, sz, vp], i32),
+        "ssa_rope": ([vp, vp, i32, i32, i32, i32, vp], i32),
+        "ssa_pack_rel_table": ([vp, i32, i32, i32, i32, vp, vp], i32),
+        "ssa_attention_ex": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -122,24 +136,55 @@ def ssa_workspace_size(B, C, H, W, num_groups, num_heads, dtype=SSA_F32) -> int:
     return int(load_library().ssa_workspace_size(B, C, H, W, num_groups, num_heads, dtype))
 
 
+def _params_list(params: dict, dtype):
+    """The 10 parameters in ABI order; a bias that is None or absent is passed
+    as NULL (that projection has no bias)."""
+    out = []
+    for k in PARAM_KEYS:
+        t = params.get(k)
+        if t is None and k in BIAS_KEYS:
+            out.append(None)
+        else:
+            out.append(_dev_tensor(t, k, dtype))
+    return out
+
+
+def _options(causal=False, rope=False, rel_table=None, dtype=None):
+    if not causal and not rope and rel_table is None:
+        return None
+    if rel_table is not None:
+        _dev_tensor(rel_table, "rel_table", dtype)
+    return SsaOptions(int(bool(causal)), int(bool(rope)), None if rel_table is None else rel_table.data_ptr())
+
+
 def ssa_forward(x: torch.Tensor, params: dict, num_groups: int, num_heads: int, out=None, workspace=None,
-                stream=None) -> torch.Tensor:
+                stream=None, causal=False, rope=False, rel_table=None) -> torch.Tensor:
     """The block, one shot (weights packed into the workspace on every call).
     x: (B, C, H, W) float32 or bfloat16 CUDA tensor; params: the 10 tensors
-    keyed as on the page, in x's dtype.  Returns out (x's dtype); out may be x."""
+    keyed as on the page, in x's dtype (a bias may be None: no bias).
+    causal / rope / rel_table ((2H-1)(2W-1), heads) select the attention
+    variants (ssa_forward_ex).  Returns out (x's dtype); out may be x."""
     lib = load_library()
     _dev_tensor(x, "x")
     dt = _dtype_code(x)
     B, C, H, W = x.shape
-    ps = [_dev_tensor(params[k], k, x.dtype) for k in PARAM_KEYS]
+    ps = _params_list(params, x.dtype)
     if out is None:
         out = torch.empty_like(x)
     _dev_tensor(out, "out", x.dtype)
-    need = ssa_workspace_size(B, C, H, W, num_groups, num_heads, dt)
+    opt = _options(causal, rope, rel_table, x.dtype)
+    if opt is None:
+        need = ssa_workspace_size(B, C, H, W, num_groups, num_heads, dt)
+    else:
+        need = int(lib.ssa_workspace_size_ex(B, C, H, W, num_groups, num_heads, dt, ctypes.byref(opt)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
-    _check(lib.ssa_forward(_ptr(x), B, C, H, W, num_groups, num_heads, *[_ptr(p) for p in ps], _ptr(out), dt,
-                           _ptr(workspace), workspace.numel(), _stream(stream)))
+    if opt is None:
+        _check(lib.ssa_forward(_ptr(x), B, C, H, W, num_groups, num_heads, *[_ptr(p) for p in ps], _ptr(out), dt,
+                               _ptr(workspace), workspace.numel(), _stream(stream)))
+    else:
+        _check(lib.ssa_forward_ex(_ptr(x), B, C, H, W, num_groups, num_heads, *[_ptr(p) for p in ps], _ptr(out),
+                                  dt, ctypes.byref(opt), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 
@@ -155,7 +200,7 @@ class SsaPlan:
         dt = _dtype_code(ref)
         self.C = ref.shape[0]
         self.num_groups, self.num_heads = num_groups, num_heads
-        self._params = {k: _dev_tensor(params[k], k, ref.dtype) for k in PARAM_KEYS}  # keep GN affine alive
+        self._params = dict(zip(PARAM_KEYS, _params_list(params, ref.dtype)))  # keep GN affine alive
         h = ctypes.c_void_p()
         _check(lib.ssa_plan_create(ctypes.byref(h), self.C, num_groups, num_heads, dt,
                                    *[_ptr(self._params[k]) for k in PARAM_KEYS], _stream(stream)))
@@ -165,19 +210,28 @@ class SsaPlan:
     def workspace_size(self, B, H, W) -> int:
         return int(load_library().ssa_plan_workspace_size(self._h, B, H, W))
 
-    def forward(self, x: torch.Tensor, out=None, workspace=None, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, out=None, workspace=None, stream=None, causal=False, rope=False,
+                rel_table=None) -> torch.Tensor:
         lib = load_library()
         _dev_tensor(x, "x", self.dtype)
         B, C, H, W = x.shape
         if out is None:
             out = torch.empty_like(x)
-        need = self.workspace_size(B, H, W)
+        opt = _options(causal, rope, rel_table, self.dtype)
+        if opt is None:
+            need = self.workspace_size(B, H, W)
+        else:
+            need = int(lib.ssa_plan_workspace_size_ex(self._h, B, H, W, ctypes.byref(opt)))
         if workspace is None:
             if self._ws is None or self._ws.numel() < need:
                 self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
             workspace = self._ws
-        _check(lib.ssa_forward_planned(self._h, _ptr(x), B, H, W, _ptr(out), _ptr(workspace),
-                                       workspace.numel(), _stream(stream)))
+        if opt is None:
+            _check(lib.ssa_forward_planned(self._h, _ptr(x), B, H, W, _ptr(out), _ptr(workspace),
+                                           workspace.numel(), _stream(stream)))
+        else:
+            _check(lib.ssa_forward_planned_ex(self._h, _ptr(x), B, H, W, _ptr(out), ctypes.byref(opt),
+                                              _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
 
     def close(self):
@@ -223,7 +277,9 @@ def ssa_pack_weights(params: dict, num_heads: int, stream=None) -> dict:
     w_o = torch.empty(C, lay["ldc"], dtype=torch.int16, device=dev)
     b_o = torch.empty(C, dtype=torch.float32, device=dev)
     keys = ("q_weight", "q_bias", "k_weight", "k_bias", "v_weight", "v_bias", "out_weight", "out_bias")
-    _check(lib.ssa_pack_weights(C, num_heads, dt, *[_ptr(_dev_tensor(params[k], k, ref.dtype)) for k in keys],
+    given = dict(zip(PARAM_KEYS, _params_list({**{k: None for k in BIAS_KEYS}, "norm_weight": ref, "norm_bias": ref,
+                                               **params}, ref.dtype)))
+    _check(lib.ssa_pack_weights(C, num_heads, dt, *[_ptr(given[k]) for k in keys],
                                 _ptr(w_qkv), _ptr(b_qkv), _ptr(w_o), _ptr(b_o), _stream(stream)))
     return {"w_qkv": w_qkv.view(torch.float16), "b_qkv": b_qkv, "w_o": w_o.view(torch.float16), "b_o": b_o}
 
@@ -251,6 +307,35 @@ def ssa_attention(q, k, vt, B: int, C: int, N: int, num_heads: int, o=None, stre
     if o is None:
         o = torch.empty(B, N, lay["ldc"], dtype=torch.float16, device=q.device)
     _check(lib.ssa_attention(_ptr(q), _ptr(k), _ptr(vt), B, C, N, num_heads, _ptr(o), _stream(stream)))
+    return o
+
+
+def ssa_rope(q, k, B: int, C: int, N: int, num_heads: int, stream=None):
+    """Rotary embedding of q and k (q/k layout) in place, token position = row."""
+    _check(load_library().ssa_rope(_ptr(q), _ptr(k), B, C, N, num_heads, _stream(stream)))
+    return q, k
+
+
+def ssa_pack_rel_table(table: torch.Tensor, H: int, W: int, num_heads: int, stream=None) -> torch.Tensor:
+    """table ((2H-1)(2W-1), heads) in float32/bfloat16 -> packed fp32
+    (heads, (2H-1)(2W-1)), each entry times log2(e)."""
+    _dev_tensor(table, "table")
+    dt = _dtype_code(table)
+    packed = torch.empty(num_heads, (2 * H - 1) * (2 * W - 1), dtype=torch.float32, device=table.device)
+    _check(load_library().ssa_pack_rel_table(_ptr(table), dt, H, W, num_heads, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def ssa_attention_ex(q, k, vt, B: int, C: int, H: int, W: int, num_heads: int, causal=False, rel_packed=None,
+                     o=None, stream=None):
+    """ssa_attention over the H x W token grid with the causal mask and the
+    packed relative-position table (ssa_pack_rel_table)."""
+    lib = load_library()
+    lay = layout(B, C, H, W, num_heads)
+    if o is None:
+        o = torch.empty(B, H * W, lay["ldc"], dtype=torch.float16, device=q.device)
+    _check(lib.ssa_attention_ex(_ptr(q), _ptr(k), _ptr(vt), B, C, H, W, num_heads, int(bool(causal)),
+                                _ptr(rel_packed), _ptr(o), _stream(stream)))
     return o
 
 

@@ -50,6 +50,9 @@ struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
   int p_tmem, p_col;  // P in tensor memory (and its column in single mode) or in shared memory
   float sl2;  // log2(e) / sqrt(d)
+  int causal;          // mask keys after the query token
+  const float *rel;    // NULL, or packed relative-position table [h][tabn] (log2 units)
+  int gh, gw, tabn;    // token grid H x W; tabn = (2H-1)(2W-1)
   int ldq;             // pair mode: row pitch of Q, K (elements)
   const uint16_t *q;   // pair mode: Q read directly into tensor memory
   uint16_t *o;
@@ -74,7 +77,44 @@ __host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot, int p
   return layout(nqb, nst, slot, p_tmem).bars + nbars(nst) * 8 + 16 + 1024;
 }
 
-template <bool SINGLE>
+// Attention variants on one thread's scores (HNDL attention operator page,
+// Masking and Relative position bias paragraphs): r holds NC x 32 raw scores
+// of query token `query` against keys k0, k0+1, ... (in order).  Each becomes
+// the base-2 logit s * log2(e)/sqrt(d) + table[dy, dx] (the table is packed
+// per head and pre-scaled by log2(e)); keys after the query under the causal
+// mask, and keys past N, become -inf.  Key (rk, ck) advances along the
+// row-major grid without divisions.
+template <int NC>
+__device__ __forceinline__ void apply_variants(uint32_t (&r)[NC][32], const AttnArgs &args, int head, int query,
+                                               int k0, float sl2) {
+  const bool qin = query < args.N;
+  const float *tab = (args.rel != nullptr && qin) ? args.rel + (long long)head * args.tabn : nullptr;
+  const int gw = args.gw;
+  const int rq = qin ? query / gw : 0, cq = qin ? query - rq * gw : 0;
+  int rk = k0 / gw, ck = k0 - (k0 / gw) * gw;
+  const int base = (rq + args.gh - 1) * (2 * gw - 1) + (cq + gw - 1);  // index at rk = ck = 0
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int key = k0 + 32 * c + i;
+      float u = __uint_as_float(r[c][i]) * sl2;
+      if (key >= args.N || (args.causal && key > query)) {
+        u = -INFINITY;
+      } else if (tab) {
+        u += __ldg(tab + base - rk * (2 * gw - 1) - ck);
+      }
+      r[c][i] = __float_as_uint(u);
+      if (++ck == gw) {
+        ck = 0;
+        ++rk;
+      }
+    }
+}
+
+// VAR: the causal mask and/or relative-position bias are on (a separate
+// instantiation, so the plain block keeps its register budget).
+template <bool SINGLE, bool VAR>
 __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
@@ -101,7 +141,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
   const int oc = blockIdx.x % args.n_oc;
   const int bh = blockIdx.y;
   const int q0 = qt * BQ;
-  const int n = args.ntiles;
+  // Under the causal mask, key tiles past the tile's last query are skipped.
+  const int n = args.causal ? min(args.ntiles, (min(q0 + BQ, args.N) - 1) / BKV + 1) : args.ntiles;
   constexpr bool single = SINGLE;
   const int nvb = 2 * args.nvr;                         // V slots per key tile
   const int nks = (args.nqb + args.kpb - 1) / args.kpb;  // K slots per key tile
@@ -298,6 +339,10 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     const uint32_t p_tile = smem_u32(sm + L.p);
     const float sl2 = args.sl2;
+    // With a mask or a bias the scores are first turned into base-2 logits
+    // (apply_variants), so the scale below becomes 1.
+    constexpr bool var = VAR;
+    const float sc = var ? 1.f : sl2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -323,6 +368,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
+      if (var) apply_variants<4>(r, args, bh % args.h, query, j * BKV, sl2);
       // Row maximum: eight independent 3-input max chains.
       float pm[8];
 #pragma unroll
@@ -334,7 +380,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
         pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
       }
       const float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      const float m_new = fmaxf(m_used, mx * sl2);
+      const float m_new = fmaxf(m_used, mx * sc);
       // Lazy rescale: a row raises its reference maximum only when the new
       // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
       // per warp (any row that needs it), because the tensor-memory accesses
@@ -351,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       }
       // p = 2^(s * log2(e)/sqrt(d) - m): one paired FMA per two scores, the
       // row sum in four paired accumulators.
-      const uint64_t c2 = f2_pack(sl2, sl2);
+      const uint64_t c2 = f2_pack(sc, sc);
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
@@ -503,6 +549,7 @@ enum {
 constexpr uint32_t P_SMEM = P_BARS + PB_COUNT * 8 + 16;
 constexpr uint32_t PMSG_BYTES = 32768 + 512 + 16;  // P tile + alpha + flags per key tile
 
+template <bool VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     attention_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const AttnArgs args) {
@@ -522,7 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = (int)(blockIdx.x >> 1) * BQ;
   const int bh = blockIdx.y;
-  const int n = (args.N + PK - 1) / PK;
+  // Under the causal mask, key tiles past the tile's last query are skipped.
+  const int n = args.causal ? min((args.N + PK - 1) / PK, (min(q0 + BQ, args.N) - 1) / PK + 1)
+                            : (args.N + PK - 1) / PK;
   const int nloads = n * 4;  // ring loads per CTA: 4 x 32 KB per key tile
 
   if (threadIdx.x == 0) {
@@ -646,6 +695,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
       const float sl2 = args.sl2;
+      constexpr bool var = VAR;  // base-2 logits first (apply_variants)
+      const float sc = var ? 1.f : sl2;
       float *xch = reinterpret_cast<float *>(sm + P_SMALL);  // [2 parity][2 half][128]
       const uint32_t r_base = mapa_u32(smem_u32(sm), 1u);
       const uint32_t r_alpha = mapa_u32(smem_u32(sm + P_ALPHA), 1u);
@@ -697,6 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
             for (int i = 0; i < 32; ++i)
               if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
         }
+        if (var) apply_variants<2>(r, args, bh % args.h, q0 + row, j * PK + half * 64, sl2);
         float pm[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -714,7 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
         if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(j & 1), ab)) { ok = false; break; }
         mx = fmaxf(mx, xch[((j & 1) * 2 + (half ^ 1)) * 128 + row]);
-        const float m_new = fmaxf(m_used, mx * sl2);
+        const float m_new = fmaxf(m_used, mx * sc);
         const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
         const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
         float alpha = 1.f;
@@ -724,7 +776,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           alpha = ex2_approx(m_used - m_new);
           m_used = m_new;
         }
-        const uint64_t c2 = f2_pack(sl2, sl2);
+        const uint64_t c2 = f2_pack(sc, sc);
         const uint64_t nm2 = f2_pack(-m_used, -m_used);
         uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[32];
@@ -959,18 +1011,24 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  cudaFuncSetAttribute(attention_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   const dim3 grid((dm.N + BQ - 1) / BQ * 2, (unsigned)BH, 1);
-  attention_pair_kernel<<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
+  if (a.causal || a.rel) {
+    cudaFuncSetAttribute(attention_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    attention_pair_kernel<true><<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
+  } else {
+    cudaFuncSetAttribute(attention_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    attention_pair_kernel<false><<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
 }  // namespace
 
 int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
-                     const KParams &kp, cudaStream_t st) {
+                     const KParams &kp, cudaStream_t st, int causal, const float *rel) {
   AttnArgs a{};
   a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
+  a.causal = causal; a.rel = rel; a.gh = dm.H; a.gw = dm.W; a.tabn = (2 * dm.H - 1) * (2 * dm.W - 1);
   a.nqb = (dm.dp + 63) / 64;
   a.ntiles = (dm.N + BKV - 1) / BKV;
   if (dm.dp == 512) {
@@ -1042,12 +1100,15 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   }
   const uint32_t smem = smem_bytes(a.nqb, nst, a.slot, a.p_tmem);
   const dim3 grid((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
+  const bool var = a.causal || a.rel;
   if (a.single) {
-    cudaFuncSetAttribute(attention_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attention_kernel<true><<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+    auto kern = var ? attention_kernel<true, true> : attention_kernel<true, false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
   } else {
-    cudaFuncSetAttribute(attention_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attention_kernel<false><<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+    auto kern = var ? attention_kernel<false, true> : attention_kernel<false, false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

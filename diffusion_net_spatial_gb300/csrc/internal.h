@@ -67,8 +67,17 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
                     const uint16_t *w_qkv, const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt,
                     const KParams &kp, cudaStream_t st);
 
+// causal: keys after the query token are masked; rel: NULL or the packed
+// relative-position table [h][(2H-1)(2W-1)] fp32 (times log2 e) over the
+// dm.H x dm.W token grid.
 int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
-                     const KParams &kp, cudaStream_t st);
+                     const KParams &kp, cudaStream_t st, int causal = 0, const float *rel = nullptr);
+
+// Rotary embedding of Q and K in place (q/k layout), token position = row.
+cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st);
+// Relative-position table [(2H-1)(2W-1)][heads] (x's dtype) -> packed.
+cudaError_t launch_rel_table_pack(int dtype, const void *table, int H, int W, int heads, float *packed,
+                                  cudaStream_t st);
 
 int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t *w_o, const float *b_o,
                     const void *x, void *out, const KParams &kp, cudaStream_t st);

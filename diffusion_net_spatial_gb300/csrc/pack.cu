@@ -52,7 +52,7 @@ __global__ void pack_kernel(int C, int h, int d, int dp, int ldc, const void *wq
         float bv_ = 0.f;
         if (e < d) {
           const void *bb = sec == 0 ? bq : (sec == 1 ? bk : bv);
-          bv_ = ld_param<DT>(bb, head * d + e);
+          bv_ = bb ? ld_param<DT>(bb, head * d + e) : 0.f;  // no bias: zero
         }
         b_qkv[row] = bv_;
       }
@@ -61,7 +61,7 @@ __global__ void pack_kernel(int C, int h, int d, int dp, int ldc, const void *wq
       const int c = (int)(j % ldc);
       const int co = (int)(j / ldc);
       w_o[j] = to_half_bits(c < C ? ld_param<DT>(wo, (long long)co * C + c) : 0.f);
-      if (c == 0) b_o[co] = ld_param<DT>(bo, co);
+      if (c == 0) b_o[co] = bo ? ld_param<DT>(bo, co) : 0.f;
     }
   }
 }

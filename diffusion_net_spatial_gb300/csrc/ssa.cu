@@ -110,10 +110,10 @@ int x_pitch(int N, ssa_dtype dt) {
 
 // Workspace layout of one forward call.
 struct WsLayout {
-  size_t ga, gs, wqkv, bqkv, wo, bo, q, k, vt, o, xpad, total;
+  size_t ga, gs, wqkv, bqkv, wo, bo, q, k, vt, o, xpad, rel, total;
 };
 
-WsLayout ws_layout(const Dims &dm, ssa_dtype dt, bool with_weights) {
+WsLayout ws_layout(const Dims &dm, ssa_dtype dt, bool with_weights, bool with_rel = false) {
   WsLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -135,6 +135,7 @@ WsLayout ws_layout(const Dims &dm, ssa_dtype dt, bool with_weights) {
   w.o = take((size_t)dm.B * dm.N * dm.ldc * 2);
   const int ldx = x_pitch(dm.N, dt);
   if (ldx != dm.N) w.xpad = take((size_t)dm.B * dm.C * ldx * esize(dt));
+  if (with_rel) w.rel = take((size_t)dm.h * (2 * dm.H - 1) * (2 * dm.W - 1) * 4);
   w.total = off;
   return w;
 }
@@ -158,10 +159,25 @@ struct Ptrs {
   const void *gw, *gb, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *bo;
 };
 
-// The four steps after packing, in stream order.
+// Variants of the attention step (all off for the block itself).
+struct Variants {
+  int causal, rope;
+  const void *rel_table;  // caller's table, x's dtype; packed into the workspace per call
+};
+
+// Checks the variants against the problem: rope needs an even head dim.
+ssa_status check_variants(const Dims &dm, const Variants &v) {
+  if (v.rope && dm.d % 2) return fail(SSA_ERR_CONSTRAINT, "rope needs an even head dim (d = %d)", dm.d);
+  if (v.rel_table && !aligned16(v.rel_table)) return fail(SSA_ERR_ALIGNMENT, "rel_pos_table must be 16-byte aligned");
+  return SSA_OK;
+}
+
+// The four steps after packing, in stream order (plus the variants' rotary
+// embedding after the projection and table packing before the attention).
 ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, const Ptrs &p,
                      const uint16_t *w_qkv, const float *b_qkv, const uint16_t *w_o, const float *b_o,
-                     uint8_t *ws, const WsLayout &wl, const KParams &kp, int num_sms, cudaStream_t st) {
+                     uint8_t *ws, const WsLayout &wl, const KParams &kp, int num_sms, cudaStream_t st,
+                     const Variants &var = Variants{0, 0, nullptr}) {
   float *ga = reinterpret_cast<float *>(ws + wl.ga);
   float *gs = reinterpret_cast<float *>(ws + wl.gs);
   uint16_t *q = reinterpret_cast<uint16_t *>(ws + wl.q);
@@ -181,7 +197,17 @@ ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, con
   int r = launch_qkv_gemm(dm, (int)dt, xq, ldx, ga, gs, w_qkv, b_qkv, q, k, vt, kp, st);
   if (r == 1) return fail(SSA_ERR_CUDA, "qkv_gemm: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "qkv_gemm launch");
-  r = launch_attention(dm, q, k, vt, o, kp, st);
+  if (var.rope) {
+    e = launch_rope(dm, q, k, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+  }
+  float *rel = nullptr;
+  if (var.rel_table) {
+    rel = reinterpret_cast<float *>(ws + wl.rel);
+    e = launch_rel_table_pack((int)dt, var.rel_table, dm.H, dm.W, dm.h, rel, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rel table pack launch");
+  }
+  r = launch_attention(dm, q, k, vt, o, kp, st, var.causal, rel);
   if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "attention launch");
   r = launch_out_proj(dm, (int)dt, o, w_o, b_o, x, out, kp, st);
@@ -253,23 +279,30 @@ size_t ssa_workspace_size(int B, int C, int H, int W, int num_groups, int num_he
   return ws_layout(make_dims(B, C, H, W, num_groups, num_heads), dtype, true).total;
 }
 
-ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
-                       const void *norm_weight, const void *norm_bias, const void *q_weight, const void *q_bias,
-                       const void *k_weight, const void *k_bias, const void *v_weight, const void *v_bias,
-                       const void *out_weight, const void *out_bias, void *out, ssa_dtype dtype, void *workspace,
-                       size_t workspace_bytes, void *stream) {
+static Variants variants_of(const ssa_options *opt) {
+  if (!opt) return Variants{0, 0, nullptr};
+  return Variants{opt->causal ? 1 : 0, opt->rope ? 1 : 0, opt->rel_pos_table};
+}
+
+static ssa_status forward_impl(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                               const void *norm_weight, const void *norm_bias, const void *q_weight,
+                               const void *q_bias, const void *k_weight, const void *k_bias, const void *v_weight,
+                               const void *v_bias, const void *out_weight, const void *out_bias, void *out,
+                               ssa_dtype dtype, const Variants &var, void *workspace, size_t workspace_bytes,
+                               void *stream) {
   ssa_status s = check_shape(B, C, H, W, num_groups, num_heads);
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
-  const void *ptrs[] = {x, norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias,
-                        v_weight, v_bias, out_weight, out_bias, out, workspace};
+  // Biases may be NULL (that projection has no bias).
+  const void *ptrs[] = {x, norm_weight, norm_bias, q_weight, k_weight, v_weight, out_weight, out, workspace};
   for (const void *p : ptrs)
     if (!p) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(SSA_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(SSA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   const Dims dm = make_dims(B, C, H, W, num_groups, num_heads);
-  const WsLayout wl = ws_layout(dm, dtype, true);
+  if ((s = check_variants(dm, var)) != SSA_OK) return s;
+  const WsLayout wl = ws_layout(dm, dtype, true, var.rel_table != nullptr);
   if (workspace_bytes < wl.total)
     return fail(SSA_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, wl.total);
   KParams kp{};
@@ -285,7 +318,33 @@ ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups
                                       out_weight, out_bias, w_qkv, b_qkv, w_o, b_o, st);
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
   const Ptrs p{norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias, v_weight, v_bias, out_weight, out_bias};
-  return run_block(dm, dtype, x, out, p, w_qkv, b_qkv, w_o, b_o, ws, wl, kp, num_sms, st);
+  return run_block(dm, dtype, x, out, p, w_qkv, b_qkv, w_o, b_o, ws, wl, kp, num_sms, st, var);
+}
+
+ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                       const void *norm_weight, const void *norm_bias, const void *q_weight, const void *q_bias,
+                       const void *k_weight, const void *k_bias, const void *v_weight, const void *v_bias,
+                       const void *out_weight, const void *out_bias, void *out, ssa_dtype dtype, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  return forward_impl(x, B, C, H, W, num_groups, num_heads, norm_weight, norm_bias, q_weight, q_bias, k_weight,
+                      k_bias, v_weight, v_bias, out_weight, out_bias, out, dtype, Variants{0, 0, nullptr}, workspace,
+                      workspace_bytes, stream);
+}
+
+size_t ssa_workspace_size_ex(int B, int C, int H, int W, int num_groups, int num_heads, ssa_dtype dtype,
+                             const ssa_options *opt) {
+  if (check_shape(B, C, H, W, num_groups, num_heads) != SSA_OK || check_dtype(dtype) != SSA_OK) return 0;
+  return ws_layout(make_dims(B, C, H, W, num_groups, num_heads), dtype, true, opt && opt->rel_pos_table).total;
+}
+
+ssa_status ssa_forward_ex(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                          const void *norm_weight, const void *norm_bias, const void *q_weight, const void *q_bias,
+                          const void *k_weight, const void *k_bias, const void *v_weight, const void *v_bias,
+                          const void *out_weight, const void *out_bias, void *out, ssa_dtype dtype,
+                          const ssa_options *opt, void *workspace, size_t workspace_bytes, void *stream) {
+  return forward_impl(x, B, C, H, W, num_groups, num_heads, norm_weight, norm_bias, q_weight, q_bias, k_weight,
+                      k_bias, v_weight, v_bias, out_weight, out_bias, out, dtype, variants_of(opt), workspace,
+                      workspace_bytes, stream);
 }
 
 ssa_status ssa_plan_create(ssa_plan **plan, int C, int num_groups, int num_heads, ssa_dtype dtype,
@@ -297,8 +356,7 @@ ssa_status ssa_plan_create(ssa_plan **plan, int C, int num_groups, int num_heads
   ssa_status s = check_shape(1, C, 1, 1, num_groups, num_heads);
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
-  const void *ptrs[] = {norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias,
-                        v_weight, v_bias, out_weight, out_bias};
+  const void *ptrs[] = {norm_weight, norm_bias, q_weight, k_weight, v_weight, out_weight};  // biases may be NULL
   for (const void *p : ptrs)
     if (!p) return fail(SSA_ERR_NULL, "a required parameter pointer is NULL");
   if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
@@ -340,8 +398,14 @@ size_t ssa_plan_workspace_size(const ssa_plan *plan, int B, int H, int W) {
   return ws_layout(make_dims(B, plan->C, H, W, plan->G, plan->h), plan->dtype, false).total;
 }
 
-ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H, int W, void *out, void *workspace,
-                               size_t workspace_bytes, void *stream) {
+size_t ssa_plan_workspace_size_ex(const ssa_plan *plan, int B, int H, int W, const ssa_options *opt) {
+  if (!plan || check_shape(B, plan->C, H, W, plan->G, plan->h) != SSA_OK) return 0;
+  return ws_layout(make_dims(B, plan->C, H, W, plan->G, plan->h), plan->dtype, false, opt && opt->rel_pos_table)
+      .total;
+}
+
+static ssa_status planned_impl(const ssa_plan *plan, const void *x, int B, int H, int W, void *out,
+                               const Variants &var, void *workspace, size_t workspace_bytes, void *stream) {
   if (!plan) return fail(SSA_ERR_NULL, "plan is NULL");
   ssa_status s = check_shape(B, plan->C, H, W, plan->G, plan->h);
   if (s != SSA_OK) return s;
@@ -350,7 +414,8 @@ ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(SSA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   const Dims dm = make_dims(B, plan->C, H, W, plan->G, plan->h);
-  const WsLayout wl = ws_layout(dm, plan->dtype, false);
+  if ((s = check_variants(dm, var)) != SSA_OK) return s;
+  const WsLayout wl = ws_layout(dm, plan->dtype, false, var.rel_table != nullptr);
   if (workspace_bytes < wl.total)
     return fail(SSA_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, wl.total);
   KParams kp{};
@@ -358,7 +423,17 @@ ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H
   if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
   const Ptrs p{plan->gw, plan->gb, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   return run_block(dm, plan->dtype, x, out, p, plan->w_qkv, plan->b_qkv, plan->w_o, plan->b_o,
-                   static_cast<uint8_t *>(workspace), wl, kp, num_sms, static_cast<cudaStream_t>(stream));
+                   static_cast<uint8_t *>(workspace), wl, kp, num_sms, static_cast<cudaStream_t>(stream), var);
+}
+
+ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H, int W, void *out, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+  return planned_impl(plan, x, B, H, W, out, Variants{0, 0, nullptr}, workspace, workspace_bytes, stream);
+}
+
+ssa_status ssa_forward_planned_ex(const ssa_plan *plan, const void *x, int B, int H, int W, void *out,
+                                  const ssa_options *opt, void *workspace, size_t workspace_bytes, void *stream) {
+  return planned_impl(plan, x, B, H, W, out, variants_of(opt), workspace, workspace_bytes, stream);
 }
 
 void ssa_plan_destroy(ssa_plan *plan) {
@@ -391,8 +466,7 @@ ssa_status ssa_pack_weights(int C, int num_heads, ssa_dtype dtype, const void *q
   ssa_status s = check_shape(1, C, 1, 1, 0, num_heads);
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
-  const void *ptrs[] = {q_weight, q_bias, k_weight, k_bias, v_weight, v_bias, out_weight, out_bias,
-                        w_qkv, b_qkv, w_o, b_o};
+  const void *ptrs[] = {q_weight, k_weight, v_weight, out_weight, w_qkv, b_qkv, w_o, b_o};  // biases may be NULL
   for (const void *p : ptrs)
     if (!p) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   const Dims dm = make_dims(1, C, 1, 1, 1, num_heads);
@@ -438,6 +512,48 @@ ssa_status ssa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v
   if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
   const Dims dm = make_dims(B, C, N, 1, 1, num_heads);
   const int r = launch_attention(dm, q, k, vt, o, kp, static_cast<cudaStream_t>(stream));
+  if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
+  if (r) return cuda_fail(cudaGetLastError(), "attention launch");
+  return SSA_OK;
+}
+
+ssa_status ssa_rope(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, void *stream) {
+  if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
+  ssa_status s = check_shape(B, C, N, 1, 0, num_heads);
+  if (s != SSA_OK) return s;
+  if (!q || !k) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  const Dims dm = make_dims(B, C, N, 1, 1, num_heads);
+  if (dm.d % 2) return fail(SSA_ERR_CONSTRAINT, "rope needs an even head dim (d = %d)", dm.d);
+  if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
+  const cudaError_t e = launch_rope(dm, q, k, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSA_OK : cuda_fail(e, "rope launch");
+}
+
+ssa_status ssa_pack_rel_table(const void *table, ssa_dtype dtype, int H, int W, int num_heads, float *packed,
+                              void *stream) {
+  if (H <= 0 || W <= 0 || num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "sizes must be positive");
+  ssa_status s = check_dtype(dtype);
+  if (s != SSA_OK) return s;
+  if (!table || !packed) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
+  const cudaError_t e = launch_rel_table_pack((int)dtype, table, H, W, num_heads, packed,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSA_OK : cuda_fail(e, "rel table pack launch");
+}
+
+ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int B, int C, int H, int W,
+                            int num_heads, int causal, const float *rel_packed, uint16_t *o, void *stream) {
+  if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
+  ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s != SSA_OK) return s;
+  if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
+    return fail(SSA_ERR_ALIGNMENT, "q, k, vt and o must be 16-byte aligned");
+  KParams kp{};
+  int num_sms = 0;
+  if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
+  const Dims dm = make_dims(B, C, H, W, 1, num_heads);
+  const int r = launch_attention(dm, q, k, vt, o, kp, static_cast<cudaStream_t>(stream), causal ? 1 : 0, rel_packed);
   if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "attention launch");
   return SSA_OK;

@@ -64,7 +64,9 @@ size_t ssa_workspace_size(int B, int C, int H, int W, int num_groups, int num_he
                           ssa_dtype dtype);
 
 /* One-shot forward of the whole block (the page's f(x, params, num_groups,
- * num_heads)).  Packs the weights into `workspace` on every call, then runs
+ * num_heads)).  q_bias, k_bias, v_bias and out_bias may be NULL: that
+ * projection then has no bias (the HNDL attention operator page's qkv_bias /
+ * out_bias flags; the block's own definition always has all four).  Packs the weights into `workspace` on every call, then runs
  * GN statistics -> QKV projection (GN affine + NCHW->token transpose fused in
  * its prologue) -> flash attention -> output projection (bias, residual and
  * NCHW store fused in its epilogue).  `out` may equal `x` (in place);
@@ -81,7 +83,8 @@ ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups
 
 /* Steady state: the parameters are constants of a module.  ssa_plan_create
  * packs them once into device memory that the plan owns (cudaMalloc here and
- * only here; freed by ssa_plan_destroy) and enqueues the pack on `stream`. */
+ * only here; freed by ssa_plan_destroy) and enqueues the pack on `stream`.
+ * The four biases may be NULL (no bias), as for ssa_forward. */
 ssa_status ssa_plan_create(ssa_plan **plan, int C, int num_groups, int num_heads, ssa_dtype dtype,
                            const void *norm_weight, const void *norm_bias,
                            const void *q_weight, const void *q_bias,
@@ -145,7 +148,8 @@ ssa_status ssa_gn_stats(const void *x, int B, int C, int N, int num_groups, ssa_
                         const void *norm_weight, const void *norm_bias,
                         float *mean, float *rstd, float *gn_scale, float *gn_shift, void *stream);
 
-/* Cast and pack the projection weights into the layouts above. */
+/* Cast and pack the projection weights into the layouts above (a NULL bias
+ * packs as zeros). */
 ssa_status ssa_pack_weights(int C, int num_heads, ssa_dtype dtype,
                             const void *q_weight, const void *q_bias,
                             const void *k_weight, const void *k_bias,
@@ -171,6 +175,65 @@ ssa_status ssa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v
 ssa_status ssa_out_project(const uint16_t *o, const uint16_t *w_o, const float *b_o,
                            const void *x, int B, int C, int H, int W, ssa_dtype dtype,
                            void *out, void *stream);
+
+/* ------------------------------------------------------------ variants --- */
+
+/* Attention variants of the HNDL "attention" operator page (parameter table
+ * and its Masking, Relative position bias and Rotary embeddings paragraphs),
+ * applied to the block's token sequence: T = H*W tokens, token t = pixel
+ * (t / W, t % W).  The block's own definition has none of them; an all-zero
+ * ssa_options (or NULL) is the block.  A = softmax(Q K^T / sqrt(d) + bias +
+ * mask) per head, after the optional rotation of Q and K. */
+typedef struct ssa_options {
+    int causal;                /* 1: token t attends only to tokens <= t (the strictly
+                                  upper triangle of the scores is -inf) */
+    int rope;                  /* 1: rotate each Q and K head by its token position,
+                                  rotate-half convention over the full head dim, base
+                                  10000, angles in fp32; needs an even head dim
+                                  (SSA_ERR_CONSTRAINT otherwise) */
+    const void *rel_pos_table; /* NULL, or the learned 2-D relative-position bias table
+                                  [(2H-1)*(2W-1)][num_heads] in x's dtype (device,
+                                  16-byte aligned): entry ((rq - rk + H - 1) * (2W - 1)
+                                  + (cq - ck + W - 1), j) is added to head j's scaled
+                                  logit of query (rq, cq) and key (rk, ck) */
+} ssa_options;
+
+/* Workspace of ssa_forward_ex (ssa_workspace_size plus the packed table). */
+size_t ssa_workspace_size_ex(int B, int C, int H, int W, int num_groups, int num_heads,
+                             ssa_dtype dtype, const ssa_options *opt);
+
+/* ssa_forward with the variants: the rotation runs after the projection (in
+ * place on Q and K), the table is packed into the workspace, and the
+ * attention kernels add the bias and apply the mask to their logits, skipping
+ * key tiles that the causal mask removes entirely. */
+ssa_status ssa_forward_ex(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
+                          const void *norm_weight, const void *norm_bias,
+                          const void *q_weight, const void *q_bias,
+                          const void *k_weight, const void *k_bias,
+                          const void *v_weight, const void *v_bias,
+                          const void *out_weight, const void *out_bias,
+                          void *out, ssa_dtype dtype, const ssa_options *opt,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Planned form of ssa_forward_ex (the table is packed into the workspace on
+ * every call; it is small). */
+size_t ssa_plan_workspace_size_ex(const ssa_plan *plan, int B, int H, int W, const ssa_options *opt);
+ssa_status ssa_forward_planned_ex(const ssa_plan *plan, const void *x, int B, int H, int W, void *out,
+                                  const ssa_options *opt, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/* Step entry points of the variants.
+ * ssa_rope: rotates q and k (q/k layout above, N tokens) in place.
+ * ssa_pack_rel_table: table [(2H-1)(2W-1)][num_heads] (x's dtype) ->
+ *   packed [num_heads][(2H-1)(2W-1)] fp32, each entry times log2(e).
+ * ssa_attention_ex: ssa_attention over the H x W token grid with the causal
+ *   mask (0/1) and the packed table (NULL: none). */
+ssa_status ssa_rope(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, void *stream);
+ssa_status ssa_pack_rel_table(const void *table, ssa_dtype dtype, int H, int W, int num_heads,
+                              float *packed, void *stream);
+ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t *vt,
+                            int B, int C, int H, int W, int num_heads, int causal,
+                            const float *rel_packed, uint16_t *o, void *stream);
 
 /* --------------------------------------------------------- diagnostics --- */
 

@@ -1,0 +1,142 @@
+"""GPU parity of the attention variants (HNDL "attention" operator page:
+bias flags, causal mask, rotary embedding, 2-D relative position bias) against
+the fp64 oracle, through the C ABI (ssa_forward_ex / ssa_forward_planned_ex
+and the step entry points).
+
+Tolerances as for the block (branch relative L2 <= 1e-2, max |delta| of out
+<= 5e-2).  The rotary angles are built in fp32 on the GPU (as the page
+prescribes) and exactly in the oracle; at the largest position here
+(16383 * theta_0) the fp32 angle is off by at most ~1e-3 rad, well inside the
+tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from diffusion_net_spatial_gb300 import workloads as wls
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 5e-2
+
+
+@pytest.fixture(scope="module")
+def ssa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_net_spatial_gb300 as m
+    m.load_library()
+    return m
+
+
+def _inputs(B, C, H, W, G, h, dtype, seed):
+    wl = wls.custom("variant", B=B, C=C, H=H, W=W, num_groups=G, num_heads=h, dtype=dtype, seed=seed)
+    x, p, qidx = wls.make_inputs(wl)
+    g = torch.Generator().manual_seed(seed + 99)
+    rel = ((torch.rand((2 * H - 1) * (2 * W - 1), h, generator=g) * 2 - 1) * 1.5).to(x.dtype)
+    return wl, x, p, rel
+
+
+def _check(ssa, out, x, p, wl, qidx=None, **kw):
+    B, C = x.shape[:2]
+    ref, y = oracle.block(x, p, wl.num_groups, wl.num_heads, qidx=qidx, **kw)
+    got = out.double().cpu().numpy().reshape(B, C, -1)
+    if qidx is not None:
+        got = got[:, :, qidx]
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(y), 1e-30)
+    mx = np.abs(got - ref).max()
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+    return rel, mx
+
+
+SHAPES = [
+    # name, B, C, H, W, G, h, dtype           attention mode
+    ("d64", 1, 128, 12, 20, 8, 2, "f32"),     # single, N = 240 (ragged)
+    ("d40", 1, 80, 9, 15, 8, 2, "f32"),       # single, d = 40 -> 48, N = 135
+    ("d320", 1, 320, 10, 10, 16, 1, "f32"),   # double (two 160-wide O halves)
+    ("d512", 1, 512, 12, 25, 32, 1, "f32"),   # pair, N = 300 (three 128-key tiles, ragged)
+    ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
+]
+VARIANTS = ["no_bias", "causal", "rope", "rel", "causal_rel", "all"]
+
+
+def _kw(variant, rel):
+    return {"causal": variant in ("causal", "causal_rel", "all"), "rope": variant in ("rope", "all"),
+            "rel_table": rel if variant in ("rel", "causal_rel", "all") else None}
+
+
+@pytest.mark.parametrize("name,B,C,H,W,G,h,dt", SHAPES, ids=[s[0] for s in SHAPES])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variant_parity(ssa, name, B, C, H, W, G, h, dt, variant):
+    wl, x, p, rel = _inputs(B, C, H, W, G, h, dt, seed=B * 1000 + C + H)
+    if variant in ("no_bias", "all"):
+        for k in ("q_bias", "k_bias", "v_bias", "out_bias"):
+            p[k] = None
+    kw = _kw(variant, rel)
+    xd = x.cuda()
+    pd = {k: (None if v is None else v.cuda()) for k, v in p.items()}
+    reld = None if kw["rel_table"] is None else kw["rel_table"].cuda()
+    out = ssa.ssa_forward(xd, pd, G, h, causal=kw["causal"], rope=kw["rope"], rel_table=reld)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    okw = dict(kw)
+    okw["rel_table"] = None if kw["rel_table"] is None else kw["rel_table"].double().numpy()
+    _check(ssa, out, x, p, wl, **okw)
+
+
+def test_planned_variants_match_one_shot(ssa):
+    wl, x, p, rel = _inputs(2, 128, 10, 14, 8, 4, "f32", seed=5)
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    plan = ssa.SsaPlan(pd, 8, 4)
+    try:
+        a = plan.forward(xd, causal=True, rope=True, rel_table=rel.cuda())
+        b = ssa.ssa_forward(xd, pd, 8, 4, causal=True, rope=True, rel_table=rel.cuda())
+        assert ssa.ssa_get_device_status() == 0
+        assert torch.equal(a, b)
+    finally:
+        plan.close()
+
+
+@pytest.mark.parametrize("name", ["unet-l1", "vae16384"])
+def test_named_workload_causal_rel(ssa, name):
+    """The two largest workloads with the causal mask and a relative-position
+    table over their full grids (64 x 64 with 8 heads; 128 x 128 with one
+    head of 512); the oracle evaluates a seeded sample of 128 query pixels."""
+    wl = wls.WORKLOADS[name]
+    x, p, _ = wls.make_inputs(wl)
+    g = torch.Generator().manual_seed(17)
+    rel = ((torch.rand((2 * wl.H - 1) * (2 * wl.W - 1), wl.num_heads, generator=g) * 2 - 1)).to(x.dtype)
+    qidx = np.sort(torch.randperm(wl.N, generator=g)[:128].numpy())
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads, causal=True, rel_table=rel.cuda())
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    _check(ssa, out, x, p, wl, qidx=qidx, causal=True, rel_table=rel.double().numpy())
+
+
+def test_rope_step_against_oracle(ssa):
+    """ssa_rope alone on the GPU's own Q/K against the oracle's rotation."""
+    B, C, H, W, h = 1, 128, 16, 16, 2
+    wl, x, p, _ = _inputs(B, C, H, W, 8, h, "f32", seed=3)
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    _, _, a, s = ssa.ssa_gn_stats(xd, 8, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, h)
+    q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], h)
+    d = C // h
+    q0 = q[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, H * W, C)
+    ssa.ssa_rope(q, k, B, C, H * W, h)
+    assert ssa.ssa_get_device_status() == 0
+    q1 = q[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, H * W, C)
+    ref = oracle.rope(q0, h)
+    # fp16 storage of the rotated values: relative 2^-11 per element
+    np.testing.assert_allclose(q1, ref, rtol=2e-3, atol=2e-3)
+
+
+def test_rope_rejects_odd_head_dim(ssa):
+    wl, x, p, _ = _inputs(1, 48, 4, 4, 4, 16, "f32", seed=4)  # d = 3
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_forward(x.cuda(), {k: v.cuda() for k, v in p.items()}, 4, 16, rope=True)
+    assert e.value.status == 1
