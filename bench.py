@@ -352,6 +352,37 @@ def run_ours(args, rank, world, local):
     roof["peak_source"] = (f"{peaks['source']} bf16 dense burst (fp16 operands: same nominal tensor rate)"
                            if roof["bound"] == "tensor" else f"{peaks['source']} HBM copy")
 
+    # ---- attention variants (HNDL attention operator page) through the same
+    # planned entry point: causal mask, rotary embedding, relative-position
+    # table, and all three together.  Reported as ms per block; the block
+    # itself stays the headline.
+    g = torch.Generator().manual_seed(wl.seed + 1234)
+    rel = ((torch.rand((2 * wl.H - 1) * (2 * wl.W - 1), wl.num_heads, generator=g) * 2 - 1)).to(xd.dtype)
+    with torch.cuda.stream(stream):
+        reld = rel.to(dev)
+    var_kw = {"causal": {"causal": True}, "rope": {"rope": True}, "rel_pos_bias": {"rel_table": reld},
+              "causal+rope+rel_pos_bias": {"causal": True, "rope": True, "rel_table": reld}}
+    var_ms = {}
+    for vname, kw in var_kw.items():
+        vws = torch.empty(max(plan.workspace_size(wl.B, wl.H, wl.W) * 2, 1 << 20), dtype=torch.uint8, device=dev)
+        tv = []
+        with torch.cuda.stream(stream):
+            for i in range(kb + 2):
+                flush.fill_(i & 0xFF)
+                torch.cuda._sleep(HOST_LEAD_CYCLES)
+                ev0 = torch.cuda.Event(enable_timing=True)
+                ev1 = torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                plan.forward(xd, out=out, workspace=vws, stream=stream, **kw)
+                ev1.record(stream)
+                if i >= 2:
+                    tv.append((ev0, ev1))
+        torch.cuda.synchronize(dev)
+        st = ssa.ssa_get_device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} in variant {vname}: {ssa.ssa_last_error_string()}")
+        var_ms[vname] = statistics.mean(a.elapsed_time(b) for a, b in tv)
+
     # ---- end to end through the public API with host buffers
     x_host = x.pin_memory()
     out_host = torch.empty(x.shape, dtype=x.dtype).pin_memory()
@@ -385,6 +416,7 @@ def run_ours(args, rank, world, local):
         "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
         "pct_of_bf16_sustained_peak": tflops / peaks["bf16_tflops_sustained"],
         "kernels_ms": kern_ms,
+        "variants_ms": var_ms,
         "roofline": roof,
         "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes},
         "gpu_launches": K * ssa.ssa_launches_per_forward(True),

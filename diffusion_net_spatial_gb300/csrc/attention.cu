@@ -78,43 +78,100 @@ __host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot, int p
 }
 
 // Attention variants on one thread's scores (HNDL attention operator page,
-// Masking and Relative position bias paragraphs): r holds NC x 32 raw scores
-// of query token `query` against keys k0, k0+1, ... (in order).  Each becomes
-// the base-2 logit s * log2(e)/sqrt(d) + table[dy, dx] (the table is packed
-// per head and pre-scaled by log2(e)); keys after the query under the causal
-// mask, and keys past N, become -inf.  Key (rk, ck) advances along the
-// row-major grid without divisions.
-template <int NC>
-__device__ __forceinline__ void apply_variants(uint32_t (&r)[NC][32], const AttnArgs &args, int head, int query,
-                                               int k0, float sl2) {
+// Masking and Relative position bias paragraphs).  r holds NC chunks of 32 raw
+// scores of query token `query` (row `lane` of a warp whose 32 queries are
+// consecutive tokens) against keys k0 + 32c + i.
+//  * causal: keys after the query become -inf (only chunks that reach past
+//    the query are touched);
+//  * relative-position table (packed per head, pre-scaled by log2 e): each
+//    score becomes the base-2 logit s * log2(e)/sqrt(d) + table[dy, dx].
+//    When W is a multiple of 32, a warp's queries share one grid row and each
+//    32-key chunk lies in one grid row, so the 32 x 32 bias block is a
+//    Toeplitz slice of one table row: 63 consecutive entries, loaded once per
+//    warp (two per lane) and handed out with one shuffle per score.  Other
+//    widths read the table per score.
+// Returns true when the scores were turned into base-2 logits.
+template <int NC, bool GENERIC>
+__device__ __forceinline__ bool apply_variants(uint32_t (&r)[NC][32], const AttnArgs &args, int head, int query,
+                                               int k0, float sl2, int lane) {
+  if (args.causal) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (k0 + 32 * c + 31 > query) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (k0 + 32 * c + i > query) r[c][i] = __float_as_uint(-INFINITY);
+      }
+  }
+  if (args.rel == nullptr) return false;
+  const float *tab = args.rel + (long long)head * args.tabn;
+  const int gw = args.gw, row_len = 2 * gw - 1;
+  const int qw = query - lane;  // the warp's first query
+  if (!GENERIC) {  // W % 32 == 0 (checked at launch)
+    if (qw < args.N) {  // warp-uniform: N is a multiple of 32 here
+      const int rq = qw / gw, cq0 = qw - rq * gw;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int kc = k0 + 32 * c;
+        if (kc >= args.N) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(-INFINITY);
+          continue;
+        }
+        const int rk = kc / gw, ck0 = kc - rk * gw;
+        // entry for (lane l, key i): e0 + l - i with e0 the lane-0, key-0 entry
+        const int e0 = (rq - rk + args.gh - 1) * row_len + (cq0 - ck0 + gw - 1);
+        // An opaque copy of the lane index: the per-step lane arithmetic below
+        // is then recomputed per chunk instead of being held in 64 registers
+        // across all chunks.
+        int ln = lane;
+        asm volatile("" : "+r"(ln));
+        const float w0 = __ldg(tab + e0 - 31 + ln);             // window entries 0 .. 31
+        const float w1 = ln < 31 ? __ldg(tab + e0 + 1 + ln) : 0.f;  // window entries 32 .. 62
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          // Lane l needs window entry l - i + 31: from lane (l + 31 - i) % 32,
+          // register w0 when l <= i, else w1.  The sending lane knows its one
+          // receiver (lane + i + 1) % 32, so it picks the register: one
+          // shuffle per score.
+          const int recv = (ln + i + 1) & 31;
+          const float b = __shfl_sync(0xFFFFFFFFu, recv <= i ? w0 : w1, (ln + 31 - i) & 31);
+          r[c][i] = __float_as_uint(fmaf(__uint_as_float(r[c][i]), sl2, b));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * sl2);
+    }
+    return true;
+  }
   const bool qin = query < args.N;
-  const float *tab = (args.rel != nullptr && qin) ? args.rel + (long long)head * args.tabn : nullptr;
-  const int gw = args.gw;
   const int rq = qin ? query / gw : 0, cq = qin ? query - rq * gw : 0;
   int rk = k0 / gw, ck = k0 - (k0 / gw) * gw;
-  const int base = (rq + args.gh - 1) * (2 * gw - 1) + (cq + gw - 1);  // index at rk = ck = 0
+  const int base = (rq + args.gh - 1) * row_len + (cq + gw - 1);  // entry at rk = ck = 0
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int key = k0 + 32 * c + i;
       float u = __uint_as_float(r[c][i]) * sl2;
-      if (key >= args.N || (args.causal && key > query)) {
-        u = -INFINITY;
-      } else if (tab) {
-        u += __ldg(tab + base - rk * (2 * gw - 1) - ck);
-      }
+      if (qin && key < args.N) u += __ldg(tab + base - rk * row_len - ck);
       r[c][i] = __float_as_uint(u);
       if (++ck == gw) {
         ck = 0;
         ++rk;
       }
     }
+  return true;
 }
 
-// VAR: the causal mask and/or relative-position bias are on (a separate
-// instantiation, so the plain block keeps its register budget).
-template <bool SINGLE, bool VAR>
+// VAR: 0 plain block; 1 causal mask and/or relative-position bias with W a
+// multiple of 32 (or no table); 2 a table over another width (per-score
+// table reads).  Separate instantiations keep the plain block's register
+// budget.
+template <bool SINGLE, int VAR>
 __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
@@ -137,9 +194,13 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x / args.n_oc;
-  const int oc = blockIdx.x % args.n_oc;
-  const int bh = blockIdx.y;
+  // Under the causal mask a query tile's work grows with its index: the grid
+  // is (B*h, query tiles x O halves) and the tiles run in reverse order, so
+  // the heaviest ones start first.
+  const int nqt = (args.N + BQ - 1) / BQ;
+  const int qt = args.causal ? nqt - 1 - (int)(blockIdx.y / args.n_oc) : (int)(blockIdx.x / args.n_oc);
+  const int oc = args.causal ? (int)(blockIdx.y % args.n_oc) : (int)(blockIdx.x % args.n_oc);
+  const int bh = args.causal ? (int)blockIdx.x : (int)blockIdx.y;
   const int q0 = qt * BQ;
   // Under the causal mask, key tiles past the tile's last query are skipped.
   const int n = args.causal ? min(args.ntiles, (min(q0 + BQ, args.N) - 1) / BKV + 1) : args.ntiles;
@@ -341,8 +402,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     const float sl2 = args.sl2;
     // With a mask or a bias the scores are first turned into base-2 logits
     // (apply_variants), so the scale below becomes 1.
-    constexpr bool var = VAR;
-    const float sc = var ? 1.f : sl2;
+    constexpr bool var = VAR != 0;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -368,7 +428,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
-      if (var) apply_variants<4>(r, args, bh % args.h, query, j * BKV, sl2);
+      float sc = sl2;  // base-2 logits when the table was added
+      if (var && apply_variants<4, VAR == 2>(r, args, bh % args.h, query, j * BKV, sl2, lane)) sc = 1.f;
       // Row maximum: eight independent 3-input max chains.
       float pm[8];
 #pragma unroll
@@ -549,7 +610,7 @@ enum {
 constexpr uint32_t P_SMEM = P_BARS + PB_COUNT * 8 + 16;
 constexpr uint32_t PMSG_BYTES = 32768 + 512 + 16;  // P tile + alpha + flags per key tile
 
-template <bool VAR>
+template <int VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
     attention_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const AttnArgs args) {
@@ -567,7 +628,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   volatile uint32_t *abort_flag = tmem_slot + 1;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = (int)(blockIdx.x >> 1) * BQ;
+  const int nqt = (args.N + BQ - 1) / BQ;
+  // Under the causal mask the heaviest query tiles start first.
+  const int q0 = (args.causal ? nqt - 1 - (int)(blockIdx.x >> 1) : (int)(blockIdx.x >> 1)) * BQ;
   const int bh = blockIdx.y;
   // Under the causal mask, key tiles past the tile's last query are skipped.
   const int n = args.causal ? min((args.N + PK - 1) / PK, (min(q0 + BQ, args.N) - 1) / PK + 1)
@@ -695,8 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
       const float sl2 = args.sl2;
-      constexpr bool var = VAR;  // base-2 logits first (apply_variants)
-      const float sc = var ? 1.f : sl2;
+      constexpr bool var = VAR != 0;
       float *xch = reinterpret_cast<float *>(sm + P_SMALL);  // [2 parity][2 half][128]
       const uint32_t r_base = mapa_u32(smem_u32(sm), 1u);
       const uint32_t r_alpha = mapa_u32(smem_u32(sm + P_ALPHA), 1u);
@@ -748,7 +810,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
             for (int i = 0; i < 32; ++i)
               if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
         }
-        if (var) apply_variants<2>(r, args, bh % args.h, q0 + row, j * PK + half * 64, sl2);
+        float sc = sl2;  // base-2 logits when the table was added
+        if (var && apply_variants<2, VAR == 2>(r, args, bh % args.h, q0 + row, j * PK + half * 64, sl2, lane))
+          sc = 1.f;
         float pm[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -1012,13 +1076,10 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
       return 1;
   }
   const dim3 grid((dm.N + BQ - 1) / BQ * 2, (unsigned)BH, 1);
-  if (a.causal || a.rel) {
-    cudaFuncSetAttribute(attention_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-    attention_pair_kernel<true><<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
-  } else {
-    cudaFuncSetAttribute(attention_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-    attention_pair_kernel<false><<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
-  }
+  const int var = (a.rel && (a.gw & 31) != 0) ? 2 : ((a.causal || a.rel) ? 1 : 0);
+  auto kern = var == 2 ? attention_pair_kernel<2> : (var == 1 ? attention_pair_kernel<1> : attention_pair_kernel<0>);
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  kern<<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
@@ -1099,14 +1160,16 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
       return 1;
   }
   const uint32_t smem = smem_bytes(a.nqb, nst, a.slot, a.p_tmem);
-  const dim3 grid((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
-  const bool var = a.causal || a.rel;
+  const dim3 grid = a.causal ? dim3((unsigned)BH, (dm.N + BQ - 1) / BQ * dm.n_oc, 1)
+                             : dim3((dm.N + BQ - 1) / BQ * dm.n_oc, (unsigned)BH, 1);
+  const int var = (a.rel && (a.gw & 31) != 0) ? 2 : ((a.causal || a.rel) ? 1 : 0);
   if (a.single) {
-    auto kern = var ? attention_kernel<true, true> : attention_kernel<true, false>;
+    auto kern = var == 2 ? attention_kernel<true, 2> : (var == 1 ? attention_kernel<true, 1> : attention_kernel<true, 0>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
   } else {
-    auto kern = var ? attention_kernel<false, true> : attention_kernel<false, false>;
+    auto kern =
+        var == 2 ? attention_kernel<false, 2> : (var == 1 ? attention_kernel<false, 1> : attention_kernel<false, 0>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
   }
