@@ -65,7 +65,8 @@ def _load():
     )
     lib.ssa_oracle_forward.restype = ctypes.c_int
     lib.ssa_oracle_forward_ex.argtypes = (
-        [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ctypes.c_int, ctypes.c_int, dp] + [ip, ctypes.c_int] + [dp] * 9
+        [dp] + [ctypes.c_int] * 6 + [dp] * 10 + [ctypes.c_int, ctypes.c_int, dp, dp, dp] + [ip, ctypes.c_int] +
+        [dp] * 9
     )
     lib.ssa_oracle_forward_ex.restype = ctypes.c_int
     lib.ssa_oracle_attention_ex.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [ip, ctypes.c_int, dp,
@@ -73,6 +74,8 @@ def _load():
     lib.ssa_oracle_attention_ex.restype = None
     lib.ssa_oracle_rope.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ip]
     lib.ssa_oracle_rope.restype = None
+    lib.ssa_oracle_qk_norm.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp]
+    lib.ssa_oracle_qk_norm.restype = None
     lib.ssa_oracle_attention.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [dp, dp]
     lib.ssa_oracle_attention.restype = None
     lib.ssa_oracle_out_proj.argtypes = [dp, dp, dp] + [ctypes.c_int] * 3 + [dp]
@@ -140,14 +143,15 @@ def gn_stats(x, num_groups: int):
 
 
 def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=(), causal=False, rope=False,
-            rel_table=None):
+            rel_table=None, q_norm_weight=None, k_norm_weight=None):
     """Run the block in fp64.
 
     x: (B, C, H, W); params: the 10 tensors keyed as on the page (a bias that
     is None or absent means that projection has no bias).
     qidx: None (every pixel) or a 1-D array of pixel indices (row i*W + j)
     shared by every sample.  causal / rope / rel_table ((2H-1)(2W-1), heads)
-    select the attention variants of the HNDL attention operator page.
+    select the attention variants of the HNDL attention operator page;
+    q_norm_weight / k_norm_weight (heads, d) the query-key RMS normalisation.
     Returns a dict with 'y' (B, C, nq) = the branch image([O] Wo^T + bo) at
     those pixels, and any of 'mean', 'rstd', 'z', 'q', 'k', 'v', 'o', 'p'
     named in ``want`` ('q', 'k' after the rotary embedding when rope).
@@ -164,6 +168,12 @@ def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()
         rel = _f64(rel_table)
         if rel.shape != ((2 * H - 1) * (2 * W - 1), num_heads):
             raise ValueError("rel_table must be ((2H-1)(2W-1), heads)")
+    qg = kg = None
+    if (q_norm_weight is None) != (k_norm_weight is None):
+        raise ValueError("q_norm_weight and k_norm_weight go together")
+    if q_norm_weight is not None:
+        qg = _f64(q_norm_weight).reshape(num_heads, -1)
+        kg = _f64(k_norm_weight).reshape(num_heads, -1)
     G, nh = num_groups, num_heads
     if qidx is not None:
         qi = np.ascontiguousarray(np.asarray(qidx, dtype=np.int32))
@@ -179,7 +189,7 @@ def forward(x, params: dict, num_groups: int, num_heads: int, qidx=None, want=()
     rc = _load().ssa_oracle_forward_ex(
         _dptr(x), B, C, H, W, G, nh,
         *[_dptr(p[k]) for k in PARAM_KEYS],
-        int(bool(causal)), int(bool(rope)), _dptr(rel),
+        int(bool(causal)), int(bool(rope)), _dptr(rel), _dptr(qg), _dptr(kg),
         qptr, nq,
         _dptr(out["y"]), *[_dptr(out.get(k)) for k in ("mean", "rstd", "z", "q", "k", "v", "o", "p")])
     if rc != 0:
@@ -239,6 +249,16 @@ def rope(m, num_heads: int, pos=None):
     return m
 
 
+def qk_norm(m, num_heads: int, gamma):
+    """Query-key RMS normalisation of rows (..., C) per head: x / max(||x||,
+    1e-12) * sqrt(d) * gamma[head], in fp64; returns a new array."""
+    m = _f64(m).copy()
+    C = m.shape[-1]
+    g = _f64(gamma).reshape(num_heads, C // num_heads)
+    _load().ssa_oracle_qk_norm(_dptr(m), int(np.prod(m.shape[:-1])), C, num_heads, _dptr(g))
+    return m
+
+
 def out_proj(o, out_weight, out_bias):
     """The output projection alone, in fp64: y (B, C, nq) = image(O Wo^T + bo)."""
     o, w = _f64(o), _f64(out_weight)
@@ -272,14 +292,15 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def block(x, params: dict, num_groups: int, num_heads: int, qidx=None, causal=False, rope=False,
-          rel_table=None):
+          rel_table=None, q_norm_weight=None, k_norm_weight=None):
     """The full block with the page's dtype rule: returns (out_f64, y_f64)
     where out_f64 is x + y rounded once to x's dtype and widened back to fp64
     for comparison.  x's dtype is read from a torch tensor ('bf16' when
     torch.bfloat16) or taken as fp32 for anything else."""
     dt = "bf16" if (hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16") else "f32"
     xf = _f64(x)
-    r = forward(xf, params, num_groups, num_heads, qidx=qidx, causal=causal, rope=rope, rel_table=rel_table)
+    r = forward(xf, params, num_groups, num_heads, qidx=qidx, causal=causal, rope=rope, rel_table=rel_table,
+                q_norm_weight=q_norm_weight, k_norm_weight=k_norm_weight)
     y = r["y"]
     B, C = xf.shape[:2]
     xs = xf.reshape(B, C, -1)

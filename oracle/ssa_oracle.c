@@ -51,6 +51,10 @@
  *     (rq, cq) and key token (rk, ck) of the row-major grid, head j adds
  *     table[((rq - rk + H - 1) * (2W - 1) + (cq - ck + W - 1)) * heads + j]
  *     to the scaled logit before the softmax.
+ *   * query-key RMS normalisation (vit-pytorch simple_vit_with_qk_norm.py,
+ *     RMSNorm class): each head's Q and K rows become
+ *     x / max(||x||_2, 1e-12) * sqrt(d) * gamma[head][:], gamma [h][d] per
+ *     projection; applied before the rotation when both are on.
  */
 #include <math.h>
 #include <stdint.h>
@@ -181,6 +185,25 @@ void ssa_oracle_rope(double *m, int rows, int C, int nh, const int *pos)
     }
 }
 
+/* ---- Query-key RMS normalisation of one (rows x C) matrix, in place ------
+ * Per row and head j: x_j / max(||x_j||_2, 1e-12) * sqrt(d) * gamma[j][:]. */
+void ssa_oracle_qk_norm(double *m, int rows, int C, int nh, const double *gamma)
+{
+    const int d = C / nh;
+    const double sd = sqrt((double)d);
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        double *row = m + (long long)r * C;
+        for (int j = 0; j < nh; ++j) {
+            double ss = 0.0;
+            for (int e = 0; e < d; ++e) ss += row[j * d + e] * row[j * d + e];
+            double nrm = sqrt(ss);
+            if (nrm < 1e-12) nrm = 1e-12;
+            for (int e = 0; e < d; ++e) row[j * d + e] = row[j * d + e] / nrm * sd * gamma[j * d + e];
+        }
+    }
+}
+
 /* ---- Step 4: output projection and image() --------------------------------
  * o [B][nq][C] -> y [B][C][nq] = (o Wo^T + bo) with the pixel axis last. */
 void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, int B, int nq, int C, double *y)
@@ -210,9 +233,10 @@ void ssa_oracle_out_proj(const double *o, const double *wo, const double *bo, in
  *   q    [B][nq][C]  k, v [B][N][C]
  *   o    [B][nq][C]  concatenated head outputs
  *   p    [B][h][nq][N] softmax probabilities (only for small problems)
- * ssa_oracle_forward_ex also takes causal, rope (both 0/1) and rel (NULL or
- * the table [(2H-1)(2W-1)][h]); any bias pointer may be NULL (no bias); q and
- * k are returned after the rotation when rope is set.
+ * ssa_oracle_forward_ex also takes causal, rope (both 0/1), rel (NULL or
+ * the table [(2H-1)(2W-1)][h]) and q_gamma / k_gamma (both NULL, or the
+ * query-key RMS-norm weights [h][d]); any bias pointer may be NULL (no bias);
+ * q and k are returned after the normalisation and rotation.
  * Returns 0; -1 on a bad shape (C % G, C % h, non-positive sizes, an odd head
  * dim with rope). */
 int ssa_oracle_forward_ex(const double *x, int B, int C, int H, int W, int G, int nh,
@@ -222,6 +246,7 @@ int ssa_oracle_forward_ex(const double *x, int B, int C, int H, int W, int G, in
                           const double *wv, const double *bv,
                           const double *wo, const double *bo,
                           int causal, int rope, const double *rel,
+                          const double *q_gamma, const double *k_gamma,
                           const int *qidx, int nq,
                           double *y, double *mean_out, double *rstd_out,
                           double *z_out, double *q_out, double *k_out,
@@ -289,7 +314,13 @@ int ssa_oracle_forward_ex(const double *x, int B, int C, int H, int W, int G, in
             }
         }
 
-    /* 2b. Rotary embedding of Q and K by token position. */
+    /* 2b. Query-key RMS normalisation, then the rotary embedding of Q and K
+     *     by token position. */
+    if (q_gamma && k_gamma)
+        for (int b = 0; b < B; ++b) {
+            ssa_oracle_qk_norm(q + (long long)b * nq * C, nq, C, nh, q_gamma);
+            ssa_oracle_qk_norm(k + (long long)b * N * C, N, C, nh, k_gamma);
+        }
     if (rope)
         for (int b = 0; b < B; ++b) {
             ssa_oracle_rope(q + (long long)b * nq * C, nq, C, nh, qidx);
@@ -322,8 +353,8 @@ int ssa_oracle_forward(const double *x, int B, int C, int H, int W, int G, int n
                        double *z_out, double *q_out, double *k_out,
                        double *v_out, double *o_out, double *p_out)
 {
-    return ssa_oracle_forward_ex(x, B, C, H, W, G, nh, gw, gb, wq, bq, wk, bk, wv, bv, wo, bo, 0, 0, NULL, qidx,
-                                 nq, y, mean_out, rstd_out, z_out, q_out, k_out, v_out, o_out, p_out);
+    return ssa_oracle_forward_ex(x, B, C, H, W, G, nh, gw, gb, wq, bq, wk, bk, wv, bv, wo, bo, 0, 0, NULL, NULL,
+                                 NULL, qidx, nq, y, mean_out, rstd_out, z_out, q_out, k_out, v_out, o_out, p_out);
 }
 
 /* ---- Rounding to the dtype of x -------------------------------------------

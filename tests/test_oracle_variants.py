@@ -1,6 +1,7 @@
 """Pins for the oracle's attention variants (HNDL "attention" operator page:
 parameter table, Biases, Masking, Relative position bias and Rotary
-embeddings paragraphs), applied to the block's row-major token sequence.
+embeddings paragraphs; vit-pytorch simple_vit_with_qk_norm.py, RMSNorm
+class), applied to the block's row-major token sequence.
 
 Each variant is checked against something other than the oracle's own loops:
 a torch library composition (F.linear without bias, SDPA with is_causal or an
@@ -222,3 +223,71 @@ def test_rel_bias_brute_force_two_tokens():
         w = np.exp(np.array(s) - max(s))
         out.append(float((w / w.sum()) @ z))
     np.testing.assert_allclose(y["y"][0, 0], out, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------ query-key RMS norm ---
+# vit-pytorch simple_vit_with_qk_norm.py, RMSNorm class: F.normalize over the
+# head dim, times sqrt(d) and a learned gamma per head and dimension.
+
+def _gammas(h, d, seed):
+    g = np.random.default_rng(seed + 31)
+    return 0.5 + g.random((h, d)), 0.5 + g.random((h, d))
+
+
+def _torch_qk_route(x, p, G, h, qg, kg, rope=False, causal=False):
+    xt = torch.from_numpy(x)
+    B, C, H, W = xt.shape
+    t = {k: torch.from_numpy(v) for k, v in p.items()}
+    gn = F.group_norm(xt, G, t["norm_weight"], t["norm_bias"], eps=1e-5)
+    z = gn.flatten(2).transpose(1, 2)
+    N, d = H * W, C // h
+    q = F.linear(z, t["q_weight"], t["q_bias"]).view(B, N, h, d).transpose(1, 2)
+    k = F.linear(z, t["k_weight"], t["k_bias"]).view(B, N, h, d).transpose(1, 2)
+    v = F.linear(z, t["v_weight"], t["v_bias"]).view(B, N, h, d).transpose(1, 2)
+    q = F.normalize(q, dim=-1) * math.sqrt(d) * torch.from_numpy(qg)[None, :, None, :]
+    k = F.normalize(k, dim=-1) * math.sqrt(d) * torch.from_numpy(kg)[None, :, None, :]
+    if rope:
+        pos = torch.arange(N)
+        q = _rope_complex(q.transpose(1, 2).reshape(B, N, C), pos, h).view(B, N, h, d).transpose(1, 2)
+        k = _rope_complex(k.transpose(1, 2).reshape(B, N, C), pos, h).view(B, N, h, d).transpose(1, 2)
+    o = F.scaled_dot_product_attention(q, k, v, is_causal=causal).transpose(1, 2).reshape(B, N, C)
+    y = F.linear(o, t["out_weight"], t["out_bias"])
+    return y.transpose(1, 2).reshape(B, C, H, W).numpy()
+
+
+@pytest.mark.parametrize("B,C,H,W,G,h", SHAPES)
+@pytest.mark.parametrize("rope,causal", [(False, False), (True, False), (True, True)])
+def test_qk_norm_matches_torch_composition(B, C, H, W, G, h, rope, causal):
+    if rope and (C // h) % 2:
+        pytest.skip("odd head dim")
+    x, p = _x(B, C, H, W, seed=C + W), _params(C, seed=H + h)
+    qg, kg = _gammas(h, C // h, seed=B + C)
+    y_ref = _torch_qk_route(x, p, G, h, qg, kg, rope=rope, causal=causal)
+    y = oracle.forward(x, p, G, h, q_norm_weight=qg, k_norm_weight=kg, rope=rope, causal=causal)["y"]
+    np.testing.assert_allclose(y.reshape(y_ref.shape), y_ref, rtol=1e-10, atol=1e-10)
+
+
+def test_qk_norm_is_invariant_to_projection_scale():
+    """Normalising Q and K per head removes any positive scale of their
+    projections: scaling Wq, bq by 3 and Wk, bk by 0.25 leaves the block
+    unchanged (and it does change it without the norm)."""
+    x, p = _x(2, 8, 3, 4, 21), _params(8, 22)
+    qg, kg = _gammas(2, 4, 23)
+    s = dict(p)
+    s["q_weight"], s["q_bias"] = 3 * p["q_weight"], 3 * p["q_bias"]
+    s["k_weight"], s["k_bias"] = 0.25 * p["k_weight"], 0.25 * p["k_bias"]
+    a = oracle.forward(x, p, 2, 2, q_norm_weight=qg, k_norm_weight=kg)["y"]
+    b = oracle.forward(x, s, 2, 2, q_norm_weight=qg, k_norm_weight=kg)["y"]
+    np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-11)
+    assert np.abs(oracle.forward(x, p, 2, 2)["y"] - oracle.forward(x, s, 2, 2)["y"]).max() > 1e-3
+
+
+def test_qk_norm_rows_have_rms_gamma():
+    """With gamma = 1/sqrt(d) (the vit-pytorch initialisation) every head row
+    of the normalised Q has unit length; with gamma = 1 its RMS is 1."""
+    g = np.random.default_rng(24)
+    m = g.standard_normal((5, 12))
+    u = oracle.qk_norm(m, 3, np.full((3, 4), 1 / 2.0)).reshape(5, 3, 4)
+    np.testing.assert_allclose(np.linalg.norm(u, axis=-1), 1.0, rtol=1e-13)
+    r = oracle.qk_norm(m, 3, np.ones((3, 4))).reshape(5, 3, 4)
+    np.testing.assert_allclose(np.sqrt((r ** 2).mean(axis=-1)), 1.0, rtol=1e-13)
