@@ -360,7 +360,12 @@ def run_ours(args, rank, world, local):
     rel = ((torch.rand((2 * wl.H - 1) * (2 * wl.W - 1), wl.num_heads, generator=g) * 2 - 1)).to(xd.dtype)
     with torch.cuda.stream(stream):
         reld = rel.to(dev)
+    d = wl.C // wl.num_heads
+    with torch.cuda.stream(stream):
+        qg = (0.5 + torch.rand(wl.num_heads, d, generator=g)).to(xd.dtype).to(dev)
+        kg = (0.5 + torch.rand(wl.num_heads, d, generator=g)).to(xd.dtype).to(dev)
     var_kw = {"causal": {"causal": True}, "rope": {"rope": True}, "rel_pos_bias": {"rel_table": reld},
+              "qk_norm": {"q_norm_weight": qg, "k_norm_weight": kg},
               "causal+rope+rel_pos_bias": {"causal": True, "rope": True, "rel_table": reld}}
     var_ms = {}
     for vname, kw in var_kw.items():

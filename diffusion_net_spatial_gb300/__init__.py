@@ -29,13 +29,14 @@ EXPORTS = ("ssa_workspace_size", "ssa_forward", "ssa_plan_create", "ssa_plan_wor
            "ssa_qkv_project", "ssa_attention", "ssa_out_project", "ssa_get_device_status",
            "ssa_set_wait_timeout_ns", "ssa_debug_timeout_probe", "ssa_last_error_string",
            "ssa_launches_per_forward", "ssa_workspace_size_ex", "ssa_forward_ex", "ssa_plan_workspace_size_ex",
-           "ssa_forward_planned_ex", "ssa_rope", "ssa_pack_rel_table", "ssa_attention_ex")
+           "ssa_forward_planned_ex", "ssa_rope", "ssa_qk_norm", "ssa_pack_rel_table", "ssa_attention_ex")
 BIAS_KEYS = ("q_bias", "k_bias", "v_bias", "out_bias")
 
 
 class SsaOptions(ctypes.Structure):
     """struct ssa_options of include/ssa.h (attention variants)."""
-    _fields_ = [("causal", ctypes.c_int), ("rope", ctypes.c_int), ("rel_pos_table", ctypes.c_void_p)]
+    _fields_ = [("causal", ctypes.c_int), ("rope", ctypes.c_int), ("rel_pos_table", ctypes.c_void_p),
+                ("q_norm_weight", ctypes.c_void_p), ("k_norm_weight", ctypes.c_void_p)]
 
 
 class SsaError(RuntimeError):
@@ -78,6 +79,7 @@ def load_library():
         "ssa_plan_workspace_size_ex": ([vp, i32, i32, i32, vp], sz),
         "ssa_forward_planned_ex": ([vp, vp, i32, i32, i32, vp, vp, vp, sz, vp], i32),
         "ssa_rope": ([vp, vp, i32, i32, i32, i32, vp], i32),
+        "ssa_qk_norm": ([vp, vp, i32, i32, i32, i32, i32, vp, vp, vp], i32),
         "ssa_pack_rel_table": ([vp, i32, i32, i32, i32, vp, vp], i32),
         "ssa_attention_ex": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp], i32),
     }
@@ -149,21 +151,25 @@ def _params_list(params: dict, dtype):
     return out
 
 
-def _options(causal=False, rope=False, rel_table=None, dtype=None):
-    if not causal and not rope and rel_table is None:
+def _options(causal=False, rope=False, rel_table=None, dtype=None, q_norm_weight=None, k_norm_weight=None):
+    if not causal and not rope and rel_table is None and q_norm_weight is None and k_norm_weight is None:
         return None
-    if rel_table is not None:
-        _dev_tensor(rel_table, "rel_table", dtype)
-    return SsaOptions(int(bool(causal)), int(bool(rope)), None if rel_table is None else rel_table.data_ptr())
+    for t, n in ((rel_table, "rel_table"), (q_norm_weight, "q_norm_weight"), (k_norm_weight, "k_norm_weight")):
+        if t is not None:
+            _dev_tensor(t, n, dtype)
+    ptr = lambda t: None if t is None else t.data_ptr()
+    return SsaOptions(int(bool(causal)), int(bool(rope)), ptr(rel_table), ptr(q_norm_weight), ptr(k_norm_weight))
 
 
 def ssa_forward(x: torch.Tensor, params: dict, num_groups: int, num_heads: int, out=None, workspace=None,
-                stream=None, causal=False, rope=False, rel_table=None) -> torch.Tensor:
+                stream=None, causal=False, rope=False, rel_table=None, q_norm_weight=None,
+                k_norm_weight=None) -> torch.Tensor:
     """The block, one shot (weights packed into the workspace on every call).
     x: (B, C, H, W) float32 or bfloat16 CUDA tensor; params: the 10 tensors
     keyed as on the page, in x's dtype (a bias may be None: no bias).
     causal / rope / rel_table ((2H-1)(2W-1), heads) select the attention
-    variants (ssa_forward_ex).  Returns out (x's dtype); out may be x."""
+    variants (ssa_forward_ex); q_norm_weight / k_norm_weight (heads, d) the
+    query-key RMS normalisation.  Returns out (x's dtype); out may be x."""
     lib = load_library()
     _dev_tensor(x, "x")
     dt = _dtype_code(x)
@@ -172,7 +178,7 @@ def ssa_forward(x: torch.Tensor, params: dict, num_groups: int, num_heads: int, 
     if out is None:
         out = torch.empty_like(x)
     _dev_tensor(out, "out", x.dtype)
-    opt = _options(causal, rope, rel_table, x.dtype)
+    opt = _options(causal, rope, rel_table, x.dtype, q_norm_weight, k_norm_weight)
     if opt is None:
         need = ssa_workspace_size(B, C, H, W, num_groups, num_heads, dt)
     else:
@@ -211,13 +217,13 @@ class SsaPlan:
         return int(load_library().ssa_plan_workspace_size(self._h, B, H, W))
 
     def forward(self, x: torch.Tensor, out=None, workspace=None, stream=None, causal=False, rope=False,
-                rel_table=None) -> torch.Tensor:
+                rel_table=None, q_norm_weight=None, k_norm_weight=None) -> torch.Tensor:
         lib = load_library()
         _dev_tensor(x, "x", self.dtype)
         B, C, H, W = x.shape
         if out is None:
             out = torch.empty_like(x)
-        opt = _options(causal, rope, rel_table, self.dtype)
+        opt = _options(causal, rope, rel_table, self.dtype, q_norm_weight, k_norm_weight)
         if opt is None:
             need = self.workspace_size(B, H, W)
         else:
@@ -313,6 +319,16 @@ def ssa_attention(q, k, vt, B: int, C: int, N: int, num_heads: int, o=None, stre
 def ssa_rope(q, k, B: int, C: int, N: int, num_heads: int, stream=None):
     """Rotary embedding of q and k (q/k layout) in place, token position = row."""
     _check(load_library().ssa_rope(_ptr(q), _ptr(k), B, C, N, num_heads, _stream(stream)))
+    return q, k
+
+
+def ssa_qk_norm(q, k, B: int, C: int, N: int, num_heads: int, q_norm_weight, k_norm_weight, stream=None):
+    """Query-key RMS normalisation of q and k (q/k layout) in place."""
+    _dev_tensor(q_norm_weight, "q_norm_weight")
+    dt = _dtype_code(q_norm_weight)
+    _check(load_library().ssa_qk_norm(_ptr(q), _ptr(k), B, C, N, num_heads, dt, _ptr(q_norm_weight),
+                                      _ptr(_dev_tensor(k_norm_weight, "k_norm_weight", q_norm_weight.dtype)),
+                                      _stream(stream)))
     return q, k
 
 

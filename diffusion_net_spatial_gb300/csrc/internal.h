@@ -75,6 +75,9 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
 
 // Rotary embedding of Q and K in place (q/k layout), token position = row.
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st);
+// Query-key RMS normalisation of Q and K in place; gammas [h][d] in x's dtype.
+cudaError_t launch_qk_norm(const Dims &dm, int dtype, uint16_t *q, uint16_t *k, const void *q_gamma,
+                           const void *k_gamma, cudaStream_t st);
 // Relative-position table [(2H-1)(2W-1)][heads] (x's dtype) -> packed.
 cudaError_t launch_rel_table_pack(int dtype, const void *table, int H, int W, int heads, float *packed,
                                   cudaStream_t st);

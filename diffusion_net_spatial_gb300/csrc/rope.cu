@@ -10,6 +10,11 @@
 // As on the page the angles are built in fp32; the rotation is applied in
 // fp32 to the fp16 Q/K values and rounded back to fp16 once.
 //
+// qk_norm_kernel: query-key RMS normalisation (vit-pytorch
+// simple_vit_with_qk_norm.py, RMSNorm class): each head's Q and K rows become
+// x / max(||x||_2, 1e-12) * sqrt(d) * gamma[head][:], one warp per row, fp32
+// sum of squares, rounded back to fp16 once.
+//
 // rel_table_pack_kernel: the learned table [(2H-1)(2W-1)][heads] in x's dtype
 // becomes one fp32 row per head, pre-multiplied by log2(e) so that the
 // attention kernels add it directly to their base-2 logits.
@@ -45,6 +50,38 @@ __global__ void rope_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int
 }
 
 template <int DT>
+__device__ __forceinline__ float ld_x(const void *p, long long i) {
+  if (DT == 0) return reinterpret_cast<const float *>(p)[i];
+  const unsigned short u = reinterpret_cast<const unsigned short *>(p)[i];
+  return __uint_as_float(((uint32_t)u) << 16);
+}
+
+template <int DT>
+__global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int h, int ldq, int d,
+                               const void *qg, const void *kg) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const float sd = sqrtf((float)d);
+  for (long long wr = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); wr < 2 * rows; wr += nwarps) {
+    const int which = wr >= rows ? 1 : 0;
+    const long long row = wr - which * rows;
+    const int head = (int)((row / N) % h);
+    __half *p = reinterpret_cast<__half *>(which ? k : q) + row * ldq;
+    const void *g = which ? kg : qg;
+    float ss = 0.f;
+    for (int e = lane; e < d; e += 32) {
+      const float v = __half2float(p[e]);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    const float scale = sd / fmaxf(sqrtf(ss), 1e-12f);
+    for (int e = lane; e < d; e += 32)
+      p[e] = __float2half_rn(__half2float(p[e]) * scale * ld_x<DT>(g, (long long)head * d + e));
+  }
+}
+
+template <int DT>
 __global__ void rel_table_pack_kernel(const void *table, int entries, int heads, float *packed) {
   const long long total = (long long)entries * heads;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -74,6 +111,18 @@ int grid_for(long long work) {
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st) {
   const long long rows = (long long)dm.B * dm.h * dm.N;
   rope_kernel<<<grid_for(rows * (dm.d / 2)), 256, 0, st>>>(q, k, rows, dm.N, dm.ldq, dm.d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_norm(const Dims &dm, int dtype, uint16_t *q, uint16_t *k, const void *q_gamma,
+                           const void *k_gamma, cudaStream_t st) {
+  const long long rows = (long long)dm.B * dm.h * dm.N;
+  long long blocks = (2 * rows + 7) / 8;  // 8 warps (rows) per block
+  if (blocks > 8192) blocks = 8192;
+  if (dtype == 0)
+    qk_norm_kernel<0><<<(int)blocks, 256, 0, st>>>(q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
+  else
+    qk_norm_kernel<1><<<(int)blocks, 256, 0, st>>>(q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
   return cudaGetLastError();
 }
 

@@ -163,12 +163,15 @@ struct Ptrs {
 struct Variants {
   int causal, rope;
   const void *rel_table;  // caller's table, x's dtype; packed into the workspace per call
+  const void *q_gamma, *k_gamma;  // query-key RMS-norm weights [h][d], x's dtype (both or neither)
 };
 
 // Checks the variants against the problem: rope needs an even head dim.
 ssa_status check_variants(const Dims &dm, const Variants &v) {
   if (v.rope && dm.d % 2) return fail(SSA_ERR_CONSTRAINT, "rope needs an even head dim (d = %d)", dm.d);
   if (v.rel_table && !aligned16(v.rel_table)) return fail(SSA_ERR_ALIGNMENT, "rel_pos_table must be 16-byte aligned");
+  if ((v.q_gamma == nullptr) != (v.k_gamma == nullptr))
+    return fail(SSA_ERR_NULL, "q_norm_weight and k_norm_weight must be given together");
   return SSA_OK;
 }
 
@@ -177,7 +180,7 @@ ssa_status check_variants(const Dims &dm, const Variants &v) {
 ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, const Ptrs &p,
                      const uint16_t *w_qkv, const float *b_qkv, const uint16_t *w_o, const float *b_o,
                      uint8_t *ws, const WsLayout &wl, const KParams &kp, int num_sms, cudaStream_t st,
-                     const Variants &var = Variants{0, 0, nullptr}) {
+                     const Variants &var = Variants{0, 0, nullptr, nullptr, nullptr}) {
   float *ga = reinterpret_cast<float *>(ws + wl.ga);
   float *gs = reinterpret_cast<float *>(ws + wl.gs);
   uint16_t *q = reinterpret_cast<uint16_t *>(ws + wl.q);
@@ -197,6 +200,10 @@ ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, con
   int r = launch_qkv_gemm(dm, (int)dt, xq, ldx, ga, gs, w_qkv, b_qkv, q, k, vt, kp, st);
   if (r == 1) return fail(SSA_ERR_CUDA, "qkv_gemm: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "qkv_gemm launch");
+  if (var.q_gamma) {
+    e = launch_qk_norm(dm, (int)dt, q, k, var.q_gamma, var.k_gamma, st);
+    if (e != cudaSuccess) return cuda_fail(e, "qk norm launch");
+  }
   if (var.rope) {
     e = launch_rope(dm, q, k, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope launch");
@@ -280,8 +287,9 @@ size_t ssa_workspace_size(int B, int C, int H, int W, int num_groups, int num_he
 }
 
 static Variants variants_of(const ssa_options *opt) {
-  if (!opt) return Variants{0, 0, nullptr};
-  return Variants{opt->causal ? 1 : 0, opt->rope ? 1 : 0, opt->rel_pos_table};
+  if (!opt) return Variants{0, 0, nullptr, nullptr, nullptr};
+  return Variants{opt->causal ? 1 : 0, opt->rope ? 1 : 0, opt->rel_pos_table, opt->q_norm_weight,
+                  opt->k_norm_weight};
 }
 
 static ssa_status forward_impl(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
@@ -327,7 +335,7 @@ ssa_status ssa_forward(const void *x, int B, int C, int H, int W, int num_groups
                        const void *out_weight, const void *out_bias, void *out, ssa_dtype dtype, void *workspace,
                        size_t workspace_bytes, void *stream) {
   return forward_impl(x, B, C, H, W, num_groups, num_heads, norm_weight, norm_bias, q_weight, q_bias, k_weight,
-                      k_bias, v_weight, v_bias, out_weight, out_bias, out, dtype, Variants{0, 0, nullptr}, workspace,
+                      k_bias, v_weight, v_bias, out_weight, out_bias, out, dtype, Variants{0, 0, nullptr, nullptr, nullptr}, workspace,
                       workspace_bytes, stream);
 }
 
@@ -428,7 +436,7 @@ static ssa_status planned_impl(const ssa_plan *plan, const void *x, int B, int H
 
 ssa_status ssa_forward_planned(const ssa_plan *plan, const void *x, int B, int H, int W, void *out, void *workspace,
                                size_t workspace_bytes, void *stream) {
-  return planned_impl(plan, x, B, H, W, out, Variants{0, 0, nullptr}, workspace, workspace_bytes, stream);
+  return planned_impl(plan, x, B, H, W, out, Variants{0, 0, nullptr, nullptr, nullptr}, workspace, workspace_bytes, stream);
 }
 
 ssa_status ssa_forward_planned_ex(const ssa_plan *plan, const void *x, int B, int H, int W, void *out,
@@ -527,6 +535,20 @@ ssa_status ssa_rope(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads
   if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
   const cudaError_t e = launch_rope(dm, q, k, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSA_OK : cuda_fail(e, "rope launch");
+}
+
+ssa_status ssa_qk_norm(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, ssa_dtype dtype,
+                       const void *q_norm_weight, const void *k_norm_weight, void *stream) {
+  if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
+  ssa_status s = check_shape(B, C, N, 1, 0, num_heads);
+  if (s != SSA_OK) return s;
+  if ((s = check_dtype(dtype)) != SSA_OK) return s;
+  if (!q || !k || !q_norm_weight || !k_norm_weight) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
+  const Dims dm = make_dims(B, C, N, 1, 1, num_heads);
+  const cudaError_t e = launch_qk_norm(dm, (int)dtype, q, k, q_norm_weight, k_norm_weight,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSA_OK : cuda_fail(e, "qk norm launch");
 }
 
 ssa_status ssa_pack_rel_table(const void *table, ssa_dtype dtype, int H, int W, int num_heads, float *packed,

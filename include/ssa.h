@@ -181,7 +181,8 @@ ssa_status ssa_out_project(const uint16_t *o, const uint16_t *w_o, const float *
 /* Attention variants of the HNDL "attention" operator page (parameter table
  * and its Masking, Relative position bias and Rotary embeddings paragraphs),
  * applied to the block's token sequence: T = H*W tokens, token t = pixel
- * (t / W, t % W).  The block's own definition has none of them; an all-zero
+ * (t / W, t % W); and the query-key RMS normalisation of the vit-pytorch
+ * "simple_vit_with_qk_norm" page.  The block's own definition has none of them; an all-zero
  * ssa_options (or NULL) is the block.  A = softmax(Q K^T / sqrt(d) + bias +
  * mask) per head, after the optional rotation of Q and K. */
 typedef struct ssa_options {
@@ -196,6 +197,12 @@ typedef struct ssa_options {
                                   16-byte aligned): entry ((rq - rk + H - 1) * (2W - 1)
                                   + (cq - ck + W - 1), j) is added to head j's scaled
                                   logit of query (rq, cq) and key (rk, ck) */
+    const void *q_norm_weight; /* NULL, or (with k_norm_weight) query-key RMS normalisation
+                                  (vit-pytorch simple_vit_with_qk_norm.py, RMSNorm class):
+                                  each Q head row becomes x / max(||x||, 1e-12) * sqrt(d)
+                                  * q_norm_weight[head][:]; [num_heads][d], x's dtype,
+                                  device; applied before the rotation */
+    const void *k_norm_weight; /* the same for K */
 } ssa_options;
 
 /* Workspace of ssa_forward_ex (ssa_workspace_size plus the packed table). */
@@ -229,6 +236,9 @@ ssa_status ssa_forward_planned_ex(const ssa_plan *plan, const void *x, int B, in
  * ssa_attention_ex: ssa_attention over the H x W token grid with the causal
  *   mask (0/1) and the packed table (NULL: none). */
 ssa_status ssa_rope(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, void *stream);
+/* ssa_qk_norm: the query-key RMS normalisation of q and k in place. */
+ssa_status ssa_qk_norm(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, ssa_dtype dtype,
+                       const void *q_norm_weight, const void *k_norm_weight, void *stream);
 ssa_status ssa_pack_rel_table(const void *table, ssa_dtype dtype, int H, int W, int num_heads,
                               float *packed, void *stream);
 ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t *vt,

@@ -1,5 +1,6 @@
 """GPU parity of the attention variants (HNDL "attention" operator page:
-bias flags, causal mask, rotary embedding, 2-D relative position bias) against
+bias flags, causal mask, rotary embedding, 2-D relative position bias; the
+query-key RMS normalisation of vit-pytorch simple_vit_with_qk_norm) against
 the fp64 oracle, through the C ABI (ssa_forward_ex / ssa_forward_planned_ex
 and the step entry points).
 
@@ -36,6 +37,10 @@ def _inputs(B, C, H, W, G, h, dtype, seed):
     x, p, qidx = wls.make_inputs(wl)
     g = torch.Generator().manual_seed(seed + 99)
     rel = ((torch.rand((2 * H - 1) * (2 * W - 1), h, generator=g) * 2 - 1) * 1.5).to(x.dtype)
+    d = C // h
+    qg = (0.5 + torch.rand(h, d, generator=g)).to(x.dtype)
+    kg = (0.5 + torch.rand(h, d, generator=g)).to(x.dtype)
+    p["_qg"], p["_kg"] = qg, kg
     return wl, x, p, rel
 
 
@@ -59,12 +64,14 @@ SHAPES = [
     ("d512", 1, 512, 12, 25, 32, 1, "f32"),   # pair, N = 300 (three 128-key tiles, ragged)
     ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
 ]
-VARIANTS = ["no_bias", "causal", "rope", "rel", "causal_rel", "all"]
+VARIANTS = ["no_bias", "causal", "rope", "rel", "causal_rel", "qk_norm", "qk_norm_rope", "all"]
 
 
-def _kw(variant, rel):
-    return {"causal": variant in ("causal", "causal_rel", "all"), "rope": variant in ("rope", "all"),
-            "rel_table": rel if variant in ("rel", "causal_rel", "all") else None}
+def _kw(variant, rel, p):
+    qn = variant in ("qk_norm", "qk_norm_rope", "all")
+    return {"causal": variant in ("causal", "causal_rel", "all"), "rope": variant in ("rope", "qk_norm_rope", "all"),
+            "rel_table": rel if variant in ("rel", "causal_rel", "all") else None,
+            "q_norm_weight": p["_qg"] if qn else None, "k_norm_weight": p["_kg"] if qn else None}
 
 
 @pytest.mark.parametrize("name,B,C,H,W,G,h,dt", SHAPES, ids=[s[0] for s in SHAPES])
@@ -74,25 +81,28 @@ def test_variant_parity(ssa, name, B, C, H, W, G, h, dt, variant):
     if variant in ("no_bias", "all"):
         for k in ("q_bias", "k_bias", "v_bias", "out_bias"):
             p[k] = None
-    kw = _kw(variant, rel)
+    kw = _kw(variant, rel, p)
+    p = {k: v for k, v in p.items() if not k.startswith("_")}
     xd = x.cuda()
     pd = {k: (None if v is None else v.cuda()) for k, v in p.items()}
-    reld = None if kw["rel_table"] is None else kw["rel_table"].cuda()
-    out = ssa.ssa_forward(xd, pd, G, h, causal=kw["causal"], rope=kw["rope"], rel_table=reld)
+    dev = {k: (None if v is None or isinstance(v, bool) else v.cuda()) for k, v in kw.items()}
+    out = ssa.ssa_forward(xd, pd, G, h, causal=kw["causal"], rope=kw["rope"], rel_table=dev["rel_table"],
+                          q_norm_weight=dev["q_norm_weight"], k_norm_weight=dev["k_norm_weight"])
     assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
-    okw = dict(kw)
-    okw["rel_table"] = None if kw["rel_table"] is None else kw["rel_table"].double().numpy()
+    okw = {k: (v.double().numpy() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
     _check(ssa, out, x, p, wl, **okw)
 
 
 def test_planned_variants_match_one_shot(ssa):
     wl, x, p, rel = _inputs(2, 128, 10, 14, 8, 4, "f32", seed=5)
+    qg, kg = p.pop("_qg").cuda(), p.pop("_kg").cuda()
     xd = x.cuda()
     pd = {k: v.cuda() for k, v in p.items()}
     plan = ssa.SsaPlan(pd, 8, 4)
     try:
-        a = plan.forward(xd, causal=True, rope=True, rel_table=rel.cuda())
-        b = ssa.ssa_forward(xd, pd, 8, 4, causal=True, rope=True, rel_table=rel.cuda())
+        a = plan.forward(xd, causal=True, rope=True, rel_table=rel.cuda(), q_norm_weight=qg, k_norm_weight=kg)
+        b = ssa.ssa_forward(xd, pd, 8, 4, causal=True, rope=True, rel_table=rel.cuda(), q_norm_weight=qg,
+                            k_norm_weight=kg)
         assert ssa.ssa_get_device_status() == 0
         assert torch.equal(a, b)
     finally:
@@ -106,7 +116,7 @@ def test_named_workload_causal_rel(ssa, name):
     head of 512); the oracle evaluates a seeded sample of 128 query pixels."""
     wl = wls.WORKLOADS[name]
     x, p, _ = wls.make_inputs(wl)
-    g = torch.Generator().manual_seed(17)
+    g = torch.Generator().manual_seed(17)  # (the named workloads carry no QK-norm weights)
     rel = ((torch.rand((2 * wl.H - 1) * (2 * wl.W - 1), wl.num_heads, generator=g) * 2 - 1)).to(x.dtype)
     qidx = np.sort(torch.randperm(wl.N, generator=g)[:128].numpy())
     xd = x.cuda()
@@ -120,6 +130,7 @@ def test_rope_step_against_oracle(ssa):
     """ssa_rope alone on the GPU's own Q/K against the oracle's rotation."""
     B, C, H, W, h = 1, 128, 16, 16, 2
     wl, x, p, _ = _inputs(B, C, H, W, 8, h, "f32", seed=3)
+    p = {k: v for k, v in p.items() if not k.startswith("_")}
     xd = x.cuda()
     pd = {k: v.cuda() for k, v in p.items()}
     _, _, a, s = ssa.ssa_gn_stats(xd, 8, pd["norm_weight"], pd["norm_bias"])
@@ -135,8 +146,28 @@ def test_rope_step_against_oracle(ssa):
     np.testing.assert_allclose(q1, ref, rtol=2e-3, atol=2e-3)
 
 
+def test_qk_norm_step_against_oracle(ssa):
+    """ssa_qk_norm alone on the GPU's own Q/K against the oracle's norm."""
+    B, C, H, W, h = 1, 128, 8, 16, 4
+    wl, x, p, _ = _inputs(B, C, H, W, 8, h, "bf16", seed=6)
+    qg, kg = p.pop("_qg"), p.pop("_kg")
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    _, _, a, s = ssa.ssa_gn_stats(xd, 8, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, h)
+    q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], h)
+    d = C // h
+    k0 = k[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, H * W, C)
+    ssa.ssa_qk_norm(q, k, B, C, H * W, h, qg.cuda(), kg.cuda())
+    assert ssa.ssa_get_device_status() == 0
+    k1 = k[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, H * W, C)
+    ref = oracle.qk_norm(k0, h, kg.double().numpy())
+    np.testing.assert_allclose(k1, ref, rtol=3e-3, atol=3e-3)
+
+
 def test_rope_rejects_odd_head_dim(ssa):
     wl, x, p, _ = _inputs(1, 48, 4, 4, 4, 16, "f32", seed=4)  # d = 3
+    p = {k: v for k, v in p.items() if not k.startswith("_")}
     with pytest.raises(ssa.SsaError) as e:
         ssa.ssa_forward(x.cuda(), {k: v.cuda() for k, v in p.items()}, 4, 16, rope=True)
     assert e.value.status == 1
