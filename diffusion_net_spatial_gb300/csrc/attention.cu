@@ -32,6 +32,8 @@
 // Keys past N in the last tile are zero-filled by TMA and masked to -inf.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -55,6 +57,10 @@ struct AttnArgs {
   int gh, gw, tabn;    // token grid H x W; tabn = (2H-1)(2W-1)
   int ldq;             // pair mode: row pitch of Q, K (elements)
   const uint16_t *q;   // pair mode: Q read directly into tensor memory
+  int pair_split, pair_P;  // pair mode work split (see PairSplit)
+  long long pair_U;
+  float *part;         // pair mode scratch: contributors' parts of cut tiles
+  uint32_t *cnt;       // pair mode scratch: per-tile contributor counts
   uint16_t *o;
   uint32_t *err;
   uint64_t timeout_ns;
@@ -563,8 +569,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
 // ---------------------------------------------------------------------------
 // Pair mode (padded head dim 512).  O for 128 queries fills all 512 tensor-
 // memory columns, so one CTA cannot hold O and the scores at once.  A cluster
-// of two CTAs on two SMs shares one query tile and splits the work by role,
-// so the scores are computed once:
+// of two CTAs on two SMs shares one query tile at a time and splits the work
+// by role, so the scores are computed once:
 //   rank 0 (score CTA)   Q (128 x 512, fp16) in tensor-memory columns
 //                        256..511; S_j = Q K_j^T for 128 keys (A operand from
 //                        tensor memory, N = 128) into one of two 128-column
@@ -577,14 +583,27 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
 //                        st.async -- all completing one barrier there.
 //   rank 1 (output CTA)  O (128 x 512 fp32) in all 512 columns; O += P_j V_j
 //                        as two groups of N = 256 MMAs (P from shared memory,
-//                        two buffers; V^T through a ring); four warps apply
-//                        the rare rescales to O before P_j V_j; at the end
-//                        O / l is written out.
+//                        three buffers; V^T through a ring); four warps apply
+//                        the rare rescales to O before P_j V_j; eight warps
+//                        write the tile's result.
 // Two producer warps per CTA issue the TMA loads (alternate ring slots): one
 // issuing thread cannot keep a ring of 32 KB boxes busy on this GPU.  The
-// score -> output hand-off of a P tile takes about a microsecond, so the
-// output CTA keeps three P buffers, and a staging tile of the score CTA is
-// handed back as soon as its copy has landed.
+// completion of each P_j V_j is signalled to both CTAs at once (a multicast
+// commit), which hands the P buffer back to the score CTA.
+//
+// Work split.  The (sample x head, 128-query) tiles are laid end to end as
+// runs of key tiles -- one unit per key tile -- and the whole line is cut
+// into P equal pieces, one per cluster, P being the number of clusters that
+// fit on the GPU at once.  Every SM pair then has the same work and no
+// partial second wave leaves most of the GPU idle.  A cluster walks its
+// piece as segments (a query tile and a range of its key tiles).  A query
+// tile cut between clusters is finished by whichever contributor ends last:
+// each writes its unnormalised O with its row maxima and row sums to scratch
+// and counts itself in with an atomic; the last one rescales every part to
+// the common maximum, adds them to its own and writes O / l.  Nobody waits
+// for another cluster.  Without scratch (and, under the causal mask, when
+// there are at least as many tiles as clusters) each cluster takes one whole
+// tile, the heaviest first.
 constexpr int PK = 128;          // keys per tile
 constexpr int PSLOT = 32768;     // ring slot: 32 KB of swizzled K or V^T blocks
 constexpr int PNPB = 3;          // P buffers in the output CTA
@@ -594,21 +613,146 @@ constexpr int PNST_MAX = 5;
 constexpr int PTHREADS = 352;    // warps: 0, 10 producers; 1 MMA; 2-9 softmax / rescale + epilogue
 constexpr uint32_t P_RING_S = 2 * 32768;
 constexpr uint32_t P_RING_O = PNPB * 32768;
-constexpr uint32_t P_SMALL = P_RING_S + PNST_S * PSLOT;  // xch (rank 0) | alpha, flags, lsum (rank 1)
+constexpr uint32_t P_SMALL = P_RING_S + PNST_S * PSLOT;  // xch (rank 0) | alpha, flags, l, m (rank 1)
 static_assert(P_RING_O + PNST_O * PSLOT <= P_SMALL, "output CTA layout");
 constexpr uint32_t P_ALPHA = P_SMALL;                // [PNPB][128] f32
 constexpr uint32_t P_FLAGS = P_SMALL + PNPB * 512;   // [PNPB][4 quarters] u32
-constexpr uint32_t P_LSUM = P_FLAGS + PNPB * 16;     // [128] f32
-constexpr uint32_t P_BARS = P_SMALL + 2560;
-static_assert(P_LSUM + 512 <= P_BARS, "small area");
+constexpr uint32_t P_LSUM = P_FLAGS + PNPB * 16;     // [128] f32 row sums of the segment
+constexpr uint32_t P_MROW = P_LSUM + 512;            // [128] f32 row maxima (base-2 logits)
+constexpr uint32_t P_BARS = P_SMALL + 2624;
+static_assert(P_MROW + 512 <= P_BARS && 2048 <= P_BARS - P_SMALL, "small area");
 enum {
   PB_FULL = 0, PB_EMPTY = PB_FULL + PNST_MAX, PB_QREADY = PB_EMPTY + PNST_MAX, PB_SFULL = PB_QREADY + 1,
-  PB_SFREE = PB_SFULL + 2, PB_STGFREE = PB_SFREE + 2, PB_PFREE = PB_STGFREE + 2, PB_XBAR = PB_PFREE + PNPB,
-  PB_PFULL = PB_XBAR + 4, PB_OREADY = PB_PFULL + PNPB, PB_PVDONE = PB_OREADY + PNPB, PB_LFULL = PB_PVDONE + PNPB,
-  PB_OFINAL = PB_LFULL + 1, PB_DRAIN = PB_OFINAL + 1, PB_COUNT = PB_DRAIN + 1
+  PB_SFREE = PB_SFULL + 2, PB_STGFREE = PB_SFREE + 2, PB_XBAR = PB_STGFREE + 2, PB_PFULL = PB_XBAR + 4,
+  PB_OREADY = PB_PFULL + PNPB, PB_PVDONE = PB_OREADY + PNPB, PB_LFULL = PB_PVDONE + PNPB, PB_LFREE = PB_LFULL + 1,
+  PB_OFINAL = PB_LFREE + 1, PB_OFREE = PB_OFINAL + 1, PB_DRAIN = PB_OFREE + 1, PB_COUNT = PB_DRAIN + 1
 };
 constexpr uint32_t P_SMEM = P_BARS + PB_COUNT * 8 + 16;
 constexpr uint32_t PMSG_BYTES = 32768 + 512 + 16;  // P tile + alpha + flags per key tile
+constexpr uint32_t PLM_BYTES = 1024;               // l and m of a segment
+// Scratch part of one contributor: O as [32 chunks][128 rows][16 columns]
+// fp32, then the row maxima and row sums.
+constexpr int PART_O_FLOATS = 128 * 512;
+constexpr int PART_FLOATS = PART_O_FLOATS + 256;
+constexpr int PAIR_MAX_CLUSTERS = 76;  // one per SM pair of a 152-SM GPU
+
+// The work line of the pair kernel (see above).  Tiles t = 0 .. T-1: sample x
+// head t / nqt; under the causal mask the query tiles of a head run from the
+// last (heaviest) to the first, and tile i of a head has nqt - i key tiles.
+struct PairSplit {
+  int nqt;     // query tiles per head (= key tiles of an unmasked query tile)
+  int causal;
+  int split;   // 1: P equal pieces of the line; 0: cluster c takes tile c
+  int P;       // clusters
+  long long U; // units (key tiles) in all
+  __device__ __forceinline__ int n_of(int t) const { return causal ? nqt - t % nqt : nqt; }
+  __device__ __forceinline__ long long cum_of(int t) const {
+    const long long bh = t / nqt, i = t % nqt;
+    return causal ? bh * ((long long)nqt * (nqt + 1) / 2) + i * nqt - i * (i - 1) / 2 : (long long)t * nqt;
+  }
+  __device__ __forceinline__ long long ubeg(int c) const { return split ? (long long)c * U / P : cum_of(c); }
+  // The cluster whose piece holds unit u (split mode).
+  __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * P - 1) / U); }
+  __device__ int tile_of(long long u) const {
+    if (!causal) return (int)(u / nqt);
+    const long long ub = (long long)nqt * (nqt + 1) / 2;
+    const int bh = (int)(u / ub);
+    const long long r = u - bh * ub;
+    // largest i with i*nqt - i(i-1)/2 <= r
+    const double b = 2.0 * nqt + 1.0;
+    int i = (int)((b - sqrt(fmax(b * b - 8.0 * (double)r, 0.0))) * 0.5);
+    i = max(0, min(i, nqt - 1));
+    while (i + 1 < nqt && (long long)(i + 1) * nqt - (long long)(i + 1) * i / 2 <= r) ++i;
+    while (i > 0 && (long long)i * nqt - (long long)i * (i - 1) / 2 > r) --i;
+    return bh * nqt + i;
+  }
+};
+
+struct PairSeg {
+  int t, bh, q0, j0, j1, n;  // tile, its head and first query; key tiles [j0, j1) of n
+  int rot;                   // unit j of the tile is key tile (j + rot) mod n
+  long long cum;             // first unit of the tile
+};
+
+// A cluster's segments in order; every role walks the same sequence.
+struct PairWalk {
+  PairSplit sp;
+  long long u, uend, cum;
+  int t;
+  __device__ PairWalk(const PairSplit &s, int c) : sp(s) {
+    u = s.ubeg(c);
+    uend = s.ubeg(c + 1);
+    t = u < uend ? s.tile_of(u) : 0;
+    cum = s.cum_of(t);
+  }
+  __device__ __forceinline__ bool more() const { return u < uend; }
+  __device__ __forceinline__ bool next(PairSeg &g) {
+    if (u >= uend) return false;
+    const int n = sp.n_of(t);
+    g.t = t;
+    g.n = n;
+    g.cum = cum;
+    g.j0 = (int)(u - cum);
+    g.j1 = (int)min((long long)n, uend - cum);
+    g.bh = t / sp.nqt;
+    // The first contributor of a tile visits key tile (its step) mod n, so
+    // clusters that started together read the same K and V tiles at the same
+    // time (a measured few per cent faster than scattered reads).
+    g.rot = sp.split ? (int)((cum - sp.ubeg(sp.owner(cum))) % n) : 0;
+    const int i = t % sp.nqt;
+    g.q0 = (sp.causal ? sp.nqt - 1 - i : i) * BQ;
+    u = cum + g.j1;
+    cum += n;
+    ++t;
+    return true;
+  }
+};
+
+// 32 output columns e0 .. e0+31 of a warp's 32 query rows (row = lane), as
+// fp16; o_w points at column 0 of the warp's first row, rows_valid of its
+// rows exist, columns at or past d are not written.  A full block goes out
+// as 64 contiguous bytes per row: a 4 x 4 transpose of 16-byte pieces inside
+// each group of 4 lanes lets lanes 4g..4g+3 write one row per store.
+__device__ __forceinline__ void store_o32(uint16_t *o_w, int ldc, int rows_valid, int e0, int d, const float (&v)[32],
+                                          int lane) {
+  if ((d & 7) == 0 && e0 + 32 <= d) {
+    const int j4 = lane & 3, g4 = lane & ~3;
+    uint32_t a[4][4];  // a[k] = this row's 16-byte piece k (columns 8k .. 8k+7)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      // (lane j of the group, piece k) -> (lane k, piece j)
+      const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
+      const uint32_t s1 = (j4 & 1) ? a[2][m] : a[3][m];
+      const uint32_t t0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+      const uint32_t t1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+      if (j4 & 1) { a[0][m] = t0; a[2][m] = t1; } else { a[1][m] = t0; a[3][m] = t1; }
+      const uint32_t u0 = (j4 & 2) ? a[0][m] : a[2][m];
+      const uint32_t u1 = (j4 & 2) ? a[1][m] : a[3][m];
+      const uint32_t w0 = __shfl_xor_sync(0xFFFFFFFFu, u0, 2);
+      const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, u1, 2);
+      if (j4 & 2) { a[0][m] = w0; a[1][m] = w1; } else { a[2][m] = w0; a[3][m] = w1; }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const int r = g4 + ii;  // row written by this group in store ii
+      if (r < rows_valid)
+        *reinterpret_cast<uint4 *>(o_w + (long long)r * ldc + e0 + j4 * 8) =
+            make_uint4(a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
+    }
+  } else if (lane < rows_valid) {
+    uint16_t *orow = o_w + (long long)lane * ldc;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (e0 + i < d) {
+        const __half hv = __float2half_rn(v[i]);
+        orow[e0 + i] = *reinterpret_cast<const uint16_t *>(&hv);
+      }
+  }
+}
 
 template <int VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
@@ -626,16 +770,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P_BARS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + P_BARS + PB_COUNT * 8);
   volatile uint32_t *abort_flag = tmem_slot + 1;
+  volatile uint32_t *last_flag = tmem_slot + 2;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqt = (args.N + BQ - 1) / BQ;
-  // Under the causal mask the heaviest query tiles start first.
-  const int q0 = (args.causal ? nqt - 1 - (int)(blockIdx.x >> 1) : (int)(blockIdx.x >> 1)) * BQ;
-  const int bh = blockIdx.y;
-  // Under the causal mask, key tiles past the tile's last query are skipped.
-  const int n = args.causal ? min((args.N + PK - 1) / PK, (min(q0 + BQ, args.N) - 1) / PK + 1)
-                            : (args.N + PK - 1) / PK;
-  const int nloads = n * 4;  // ring loads per CTA: 4 x 32 KB per key tile
+  const int cid = (int)(blockIdx.x >> 1);
+  const PairSplit sp{(args.N + BQ - 1) / BQ, args.causal, args.pair_split, args.pair_P, args.pair_U};
+  const int G = (int)(sp.ubeg(cid + 1) - sp.ubeg(cid));  // key tiles this cluster processes
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < PNST_MAX; ++i) {
@@ -649,22 +789,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       mbar_init(&bars[PB_STGFREE + b], 1);
     }
     for (int b = 0; b < PNPB; ++b) {
-      mbar_init(&bars[PB_PFREE + b], 1);
       mbar_init(&bars[PB_PFULL + b], 1);
       mbar_init(&bars[PB_OREADY + b], 4);
       mbar_init(&bars[PB_PVDONE + b], 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars[PB_XBAR + i], 2);
     mbar_init(&bars[PB_LFULL], 1);
+    mbar_init(&bars[PB_LFREE], 1);
     mbar_init(&bars[PB_OFINAL], 1);
+    mbar_init(&bars[PB_OFREE], 8);
     mbar_init(&bars[PB_DRAIN], 1);
     *abort_flag = 0u;
     fence_barrier_init();
     if (rank == 1) {
-      // Armed for the first PNPB key tiles and for the row sums; the bytes
-      // come from the score CTA.
-      for (int b = 0; b < PNPB && b < n; ++b) mbar_arrive_expect_tx(&bars[PB_PFULL + b], PMSG_BYTES);
-      mbar_arrive_expect_tx(&bars[PB_LFULL], 512u);
+      // Armed for the first PNPB key tiles and for the first segment's row
+      // sums and maxima; the bytes come from the score CTA.
+      for (int b = 0; b < PNPB && b < G; ++b) mbar_arrive_expect_tx(&bars[PB_PFULL + b], PMSG_BYTES);
+      mbar_arrive_expect_tx(&bars[PB_LFULL], PLM_BYTES);
       tma_prefetch_desc(&vmap);
     } else {
       tma_prefetch_desc(&kmap);
@@ -680,28 +821,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, args.err, args.timeout_ns};
   const uint32_t slot16 = (uint32_t)PSLOT >> 4;
+  bool ok = true;
 
   if (warp == 0 || warp == 10) {
     // ------------------------------------------------------ TMA producers
-    // Load t goes to ring slot t mod nst; warp 0 issues the even loads, warp 10
-    // the odd ones.  Rank 0: K as [2 x 64 dims] x 128 keys per load (4 per
+    // Load L goes to ring slot L mod nst; warp 0 issues the even loads, warp
+    // 10 the odd ones.  Rank 0: K as [2 x 64 dims] x 128 keys per load (4 per
     // key tile); rank 1: V^T as [256 output dims x 64 keys] (output half 0,
     // then half 1, two key blocks each).
     if (lane == 0) {
       const int me = warp == 0 ? 0 : 1;
       const int nst = rank == 0 ? PNST_S : PNST_O;
       uint8_t *ring = sm + (rank == 0 ? P_RING_S : P_RING_O);
-      int last = -1;
-      for (int t = me; t < nloads; t += 2) {
-        const int s = t % nst, round = t / nst;
-        if (round > 0 && !mbar_wait(&bars[PB_EMPTY + s], (uint32_t)((round - 1) & 1), ab)) break;
-        mbar_arrive_expect_tx(&bars[PB_FULL + s], (uint32_t)PSLOT);
-        const int j = t >> 2, r = t & 3;
-        if (rank == 0)
-          tma_load_4d(ring + s * PSLOT, &kmap, &bars[PB_FULL + s], 0, j * PK, 2 * r, bh);
-        else
-          tma_load_3d(ring + s * PSLOT, &vmap, &bars[PB_FULL + s], j * PK + (r & 1) * 64, (r >> 1) * 256, bh);
-        last = t;
+      // A strided loop over this warp's own loads: a loop that visits every
+      // load and skips the other warp's measured markedly slower.
+      int last = -1, lbase = 0;
+      PairWalk wk(sp, cid);
+      PairSeg sg;
+      while (ok && wk.next(sg)) {
+        const int nl = (sg.j1 - sg.j0) * 4;  // lbase is a multiple of 4: the parity split holds
+        for (int t = me; t < nl; t += 2) {
+          const int L = lbase + t, s = L % nst, round = L / nst;
+          if (round > 0 && !mbar_wait(&bars[PB_EMPTY + s], (uint32_t)((round - 1) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars[PB_FULL + s], (uint32_t)PSLOT);
+          const int j = (sg.j0 + (t >> 2) + sg.rot) % sg.n, r = t & 3;
+          if (rank == 0)
+            tma_load_4d(ring + s * PSLOT, &kmap, &bars[PB_FULL + s], 0, j * PK, 2 * r, sg.bh);
+          else
+            tma_load_3d(ring + s * PSLOT, &vmap, &bars[PB_FULL + s], j * PK + (r & 1) * 64, (r >> 1) * 256, sg.bh);
+          last = L;
+        }
+        lbase += nl;
       }
       // After an abort no load may still be landing when the CTA leaves.
       if (*abort_flag)
@@ -718,33 +871,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       // MMAs issued before it.
       const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING_S));
       const uint32_t idesc = idesc_f16(BQ, PK);
-      int s = 0;
+      int s = 0, g = 0, si = 0;
       uint32_t ph = 0;
-      bool ok = mbar_wait_warp(&bars[PB_QREADY], 0, ab), issued = false;
-      for (int j = 0; j < n && ok; ++j) {
-        const int buf = j & 1, u = j >> 1;
-        if (j >= 2 && !mbar_wait_warp(&bars[PB_SFREE + buf], (uint32_t)((u - 1) & 1), ab)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_s = tmem + (uint32_t)(buf * PK);
-        for (int c = 0; c < 4 && ok; ++c) {
-          if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
+      bool issued = false;
+      PairWalk wk(sp, cid);
+      PairSeg sg;
+      while (ok && wk.next(sg)) {
+        // Q of this segment's tile is in tensor memory.
+        if (!mbar_wait_warp(&bars[PB_QREADY], (uint32_t)(si & 1), ab)) { ok = false; break; }
+        for (int j = sg.j0; j < sg.j1 && ok; ++j, ++g) {
+          const int buf = g & 1, u = g >> 1;
+          if (g >= 2 && !mbar_wait_warp(&bars[PB_SFREE + buf], (uint32_t)((u - 1) & 1), ab)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t b0 = rd + (uint64_t)(s * slot16);
-          if (elect_one()) {
+          const uint32_t d_s = tmem + (uint32_t)(buf * PK);
+          for (int c = 0; c < 4 && ok; ++c) {
+            if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t b0 = rd + (uint64_t)(s * slot16);
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // 16 dims per step; Q dims 2c' and 2c'+1 in column 256 + c'
-              mma_f16_ts(d_s, tmem + 256u + (uint32_t)((c * 8 + ks) * 8),
-                         b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), idesc, (c | ks) ? 1u : 0u);
-            mma_commit(&bars[PB_EMPTY + s]);
+              for (int ks = 0; ks < 8; ++ks)  // 16 dims per step; Q dims 2c' and 2c'+1 in column 256 + c'
+                mma_f16_ts(d_s, tmem + 256u + (uint32_t)((c * 8 + ks) * 8),
+                           b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), idesc, (c | ks) ? 1u : 0u);
+              mma_commit(&bars[PB_EMPTY + s]);
+            }
+            __syncwarp();
+            issued = true;
+            if (++s == PNST_S) { s = 0; ph ^= 1u; }
           }
-          __syncwarp();
-          issued = true;
-          if (++s == PNST_S) { s = 0; ph ^= 1u; }
+          if (ok) {
+            if (elect_one()) mma_commit(&bars[PB_SFULL + buf]);
+            __syncwarp();
+          }
         }
-        if (ok) {
-          if (elect_one()) mma_commit(&bars[PB_SFULL + buf]);
-          __syncwarp();
-        }
+        ++si;
       }
       if (!ok && issued) {
         if (elect_one()) mma_commit(&bars[PB_DRAIN]);
@@ -764,139 +924,158 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       const uint32_t r_alpha = mapa_u32(smem_u32(sm + P_ALPHA), 1u);
       const uint32_t r_flags = mapa_u32(smem_u32(sm + P_FLAGS), 1u);
       const uint32_t r_lsum = mapa_u32(smem_u32(sm + P_LSUM), 1u);
+      const uint32_t r_mrow = mapa_u32(smem_u32(sm + P_MROW), 1u);
       const uint32_t r_pfull0 = mapa_u32(smem_u32(&bars[PB_PFULL]), 1u);
       const uint32_t r_lfull = mapa_u32(smem_u32(&bars[PB_LFULL]), 1u);
-      {
-        // Q rows into tensor memory: this warp's 32 rows, dims half*256 ..
-        // +255 (rows past N are zero).
-        const bool qv = q0 + row < args.N;
-        const uint4 *qrow = reinterpret_cast<const uint4 *>(
-            args.q + ((long long)bh * args.N + (qv ? q0 + row : 0)) * args.ldq + half * 256);
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[32];
+      int g = 0, xi = 0, si = 0;
+      PairWalk wk(sp, cid);
+      PairSeg sg;
+      while (ok && wk.next(sg)) {
+        const int q0 = sg.q0, bh = sg.bh;
+        {
+          // Q rows into tensor memory: this warp's 32 rows, dims half*256 ..
+          // +255 (rows past N are zero).  The previous segment's QK^T MMAs
+          // all completed before its last scores were read.
+          const bool qv = q0 + row < args.N;
+          const uint4 *qrow = reinterpret_cast<const uint4 *>(
+              args.q + ((long long)bh * args.N + (qv ? q0 + row : 0)) * args.ldq + half * 256);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = qv ? __ldg(qrow + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+            for (int i = 0; i < 8; ++i) {
+              const uint4 v = qv ? __ldg(qrow + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+              w[4 * i] = v.x;
+              w[4 * i + 1] = v.y;
+              w[4 * i + 2] = v.z;
+              w[4 * i + 3] = v.w;
+            }
+            tmem_st32(lane_base + 256u + (uint32_t)(half * 128 + c * 32), w);
           }
-          tmem_st32(lane_base + 256u + (uint32_t)(half * 128 + c * 32), w);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[PB_QREADY]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[PB_QREADY]);
-      }
-      float m_used = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int buf = j & 1, u = j >> 1;
-        if (!mbar_wait_warp(&bars[PB_SFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t r[2][32];
-        tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64), r[0]);
-        tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64 + 32), r[1]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[PB_SFREE + buf]);
-        const int kvalid = min(PK, args.N - j * PK) - half * 64;
-        if (kvalid < 64) {
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = sg.j0; j < sg.j1; ++j, ++g, ++xi) {
+          const int buf = g & 1, u = g >> 1;
+          if (!mbar_wait_warp(&bars[PB_SFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t r[2][32];
+          tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64), r[0]);
+          tmem_ld32(lane_base + (uint32_t)(buf * PK + half * 64 + 32), r[1]);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[PB_SFREE + buf]);
+          const int kt = (j + sg.rot) % sg.n;  // key tile
+          const int kvalid = min(PK, args.N - kt * PK) - half * 64;
+          if (kvalid < 64) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
+          }
+          float sc = sl2;  // base-2 logits when the table was added
+          if (var && apply_variants<2, VAR == 2>(r, args, bh % args.h, q0 + row, kt * PK + half * 64, sl2, lane))
+            sc = 1.f;
+          float pm[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = t >> 1, o = (t & 1) * 16;
+            float m = __uint_as_float(r[c][o]);
+#pragma unroll
+            for (int i = 1; i < 15; i += 2)
+              m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
+            pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
+          }
+          float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
+          // The other half of this row (same lanes, other warp): exchange maxima.
+          xch[((xi & 1) * 2 + half) * 128 + row] = mx;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
+          if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(xi & 1), ab)) { ok = false; break; }
+          mx = fmaxf(mx, xch[((xi & 1) * 2 + (half ^ 1)) * 128 + row]);
+          const float m_new = fmaxf(m_used, mx * sc);
+          const bool need = (j > sg.j0) && (m_new > m_used + RESCALE_LOG2);
+          const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
+          float alpha = 1.f;
+          if (j == sg.j0) {
+            m_used = m_new;
+          } else if (rescale && m_new > m_used) {
+            alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+          }
+          const uint64_t c2 = f2_pack(sc, sc);
+          const uint64_t nm2 = f2_pack(-m_used, -m_used);
+          uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+          uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
-        }
-        float sc = sl2;  // base-2 logits when the table was added
-        if (var && apply_variants<2, VAR == 2>(r, args, bh % args.h, q0 + row, j * PK + half * 64, sl2, lane))
-          sc = 1.f;
-        float pm[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int c = t >> 1, o = (t & 1) * 16;
-          float m = __uint_as_float(r[c][o]);
-#pragma unroll
-          for (int i = 1; i < 15; i += 2)
-            m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
-          pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
-        }
-        float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
-        // The other half of this row (same lanes, other warp): exchange maxima.
-        xch[((j & 1) * 2 + half) * 128 + row] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
-        if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(j & 1), ab)) { ok = false; break; }
-        mx = fmaxf(mx, xch[((j & 1) * 2 + (half ^ 1)) * 128 + row]);
-        const float m_new = fmaxf(m_used, mx * sc);
-        const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
-        const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
-        float alpha = 1.f;
-        if (j == 0) {
-          m_used = m_new;
-        } else if (rescale && m_new > m_used) {
-          alpha = ex2_approx(m_used - m_new);
-          m_used = m_new;
-        }
-        const uint64_t c2 = f2_pack(sc, sc);
-        const uint64_t nm2 = f2_pack(-m_used, -m_used);
-        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float t0, t1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-            const float e0 = ex2_approx(t0);
-            const float e1 = ex2_approx(t1);
-            acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
-            pk[c * 16 + (i >> 1)] = pack_half2(e0, e1);
+            for (int i = 0; i < 32; i += 2) {
+              float t0, t1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+              const float e0 = ex2_approx(t0);
+              const float e1 = ex2_approx(t1);
+              acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
+              pk[c * 16 + (i >> 1)] = pack_half2(e0, e1);
+            }
+          float s0, s1, s2, s3;
+          f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+          f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
+          l = l * alpha + ((s0 + s1) + (s2 + s3));
+          // Staging tile `buf` is free once the copy of tile g-2 has landed;
+          // the output CTA's P buffer `pb` once its P V_{g-PNPB} is done.
+          const int pb = g % PNPB, up = g / PNPB;
+          if (g >= 2 && !mbar_wait_cluster_warp(&bars[PB_STGFREE + buf], (uint32_t)((u - 1) & 1), ab)) {
+            ok = false;
+            break;
           }
-        float s0, s1, s2, s3;
-        f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
-        f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
-        l = l * alpha + ((s0 + s1) + (s2 + s3));
-        // Staging tile `buf` is free once the copy of tile j-2 has landed;
-        // the output CTA's P buffer `pb` once its P V_{j-PNPB} is done.
-        const int pb = j % PNPB, up = j / PNPB;
-        if (j >= 2 && !mbar_wait_cluster_warp(&bars[PB_STGFREE + buf], (uint32_t)((u - 1) & 1), ab)) {
-          ok = false;
-          break;
-        }
-        if (j >= PNPB && !mbar_wait_cluster_warp(&bars[PB_PFREE + pb], (uint32_t)((up - 1) & 1), ab)) {
-          ok = false;
-          break;
-        }
-        uint8_t *stg = sm + buf * 32768 + half * 16384;  // this half's 64 keys
+          if (g >= PNPB && !mbar_wait_cluster_warp(&bars[PB_PVDONE + pb], (uint32_t)((up - 1) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          uint8_t *stg = sm + buf * 32768 + half * 16384;  // this half's 64 keys
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(smem_u32(stg) + sw128_offset((uint32_t)row, (uint32_t)ch), pk[ch * 4], pk[ch * 4 + 1],
-                       pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        const uint32_t rbar = r_pfull0 + (uint32_t)(pb * 8);
-        if (lane == 0)
-          bulk_copy_to_cluster(r_base + (uint32_t)(pb * 32768 + half * 16384 + q4 * 4096), stg + q4 * 4096, 4096u,
-                               rbar);
-        if (half == 0) {
-          st_async_b32(r_alpha + (uint32_t)((pb * 128 + row) * 4), __float_as_uint(alpha), rbar);
-          if (lane == 0) st_async_b32(r_flags + (uint32_t)((pb * 4 + q4) * 4), rescale ? 1u : 0u, rbar);
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(smem_u32(stg) + sw128_offset((uint32_t)row, (uint32_t)ch), pk[ch * 4], pk[ch * 4 + 1],
+                         pk[ch * 4 + 2], pk[ch * 4 + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t rbar = r_pfull0 + (uint32_t)(pb * 8);
+          if (lane == 0)
+            bulk_copy_to_cluster(r_base + (uint32_t)(pb * 32768 + half * 16384 + q4 * 4096), stg + q4 * 4096, 4096u,
+                                 rbar);
+          if (half == 0) {
+            st_async_b32(r_alpha + (uint32_t)((pb * 128 + row) * 4), __float_as_uint(alpha), rbar);
+            if (lane == 0) st_async_b32(r_flags + (uint32_t)((pb * 4 + q4) * 4), rescale ? 1u : 0u, rbar);
+          }
         }
-      }
-      if (ok) {
-        // Combine the two halves' row sums (exchange slot of parity n) and
-        // send them to the output CTA.
-        xch[((n & 1) * 2 + half) * 128 + row] = l;
+        if (!ok) break;
+        // End of the segment: combine the two halves' row sums and send the
+        // sums and maxima to the output CTA once it has taken the previous
+        // segment's.
+        xch[((xi & 1) * 2 + half) * 128 + row] = l;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[PB_XBAR + q4]);
-        if (mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(n & 1), ab)) {
-          l += xch[((n & 1) * 2 + (half ^ 1)) * 128 + row];
-          if (half == 0) st_async_b32(r_lsum + (uint32_t)(row * 4), __float_as_uint(l), r_lfull);
+        if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(xi & 1), ab)) { ok = false; break; }
+        l += xch[((xi & 1) * 2 + (half ^ 1)) * 128 + row];
+        ++xi;
+        if (half == 0) {
+          if (si > 0 && !mbar_wait_cluster_warp(&bars[PB_LFREE], (uint32_t)((si - 1) & 1), ab)) { ok = false; break; }
+          st_async_b32(r_lsum + (uint32_t)(row * 4), __float_as_uint(l), r_lfull);
+          st_async_b32(r_mrow + (uint32_t)(row * 4), __float_as_uint(m_used), r_lfull);
         }
+        ++si;
       }
+      // The completions of the last P V products also arrive here; this CTA
+      // stays until they have.
+      if (warp == 2 && lane == 0 && ok)
+        for (int gg = max(0, G - PNPB); gg < G; ++gg)
+          if (!mbar_wait_cluster(&bars[PB_PVDONE + gg % PNPB], (uint32_t)((gg / PNPB) & 1), ab)) break;
+      __syncwarp();
     }
   } else {
     // ==================================================== output CTA ======
@@ -905,47 +1084,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       const uint64_t pd = sdesc_k128(smem_u32(sm));
       const uint64_t rd = sdesc_k128(smem_u32(sm + P_RING_O));
       const uint32_t idesc = idesc_f16(BQ, 256);
-      int s = 0;
+      const uint32_t r_stgfree0 = mapa_u32(smem_u32(&bars[PB_STGFREE]), 0u);
+      int s = 0, g = 0, si = 0;
       uint32_t ph = 0;
-      bool ok = true, issued = false;
-      for (int j = 0; j < n && ok; ++j) {
-        const int buf = j % PNPB, u = j / PNPB;
-        if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab) ||
-            !mbar_wait_warp(&bars[PB_OREADY + buf], (uint32_t)(u & 1), ab)) {
-          ok = false;
-          break;
-        }
-        if (elect_one()) {
-          if (j + PNPB < n) mbar_arrive_expect_tx(&bars[PB_PFULL + buf], PMSG_BYTES);
-          fence_proxy_async_smem();  // P and the rescale factors came from the other CTA
-        }
-        __syncwarp();
+      bool issued = false;
+      PairWalk wk(sp, cid);
+      PairSeg sg;
+      while (ok && wk.next(sg)) {
+        // O is free once the previous segment's result has been read out.
+        if (si > 0 && !mbar_wait_warp(&bars[PB_OFREE], (uint32_t)((si - 1) & 1), ab)) { ok = false; break; }
         tc_fence_after();
-        for (int r = 0; r < 4 && ok; ++r) {
-          if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t a0 = pd + (uint64_t)(buf * 2048 + (r & 1) * 1024);
-          const uint64_t b0 = rd + (uint64_t)(s * slot16);
-          const uint32_t d_o = tmem + (uint32_t)((r >> 1) * 256);
-          const uint32_t first = (j > 0 || (r & 1) > 0) ? 1u : 0u;
+        for (int j = sg.j0; j < sg.j1 && ok; ++j, ++g) {
+          const int buf = g % PNPB, u = g / PNPB;
+          if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
+          // P_g has landed, so the score CTA's staging tile g mod 2 is free.
+          // (No ordering to publish: a relaxed arrive, which keeps this warp's
+          // issue loop short.)
+          if (elect_one() && g + 2 < G) mbar_arrive_remote_relaxed(r_stgfree0 + (uint32_t)((g & 1) * 8));
+          __syncwarp();
+          if (!mbar_wait_warp(&bars[PB_OREADY + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
           if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (first | kk) ? 1u : 0u);
-            mma_commit(&bars[PB_EMPTY + s]);
+            if (g + PNPB < G) mbar_arrive_expect_tx(&bars[PB_PFULL + buf], PMSG_BYTES);
+            fence_proxy_async_smem();  // P and the rescale factors came from the other CTA
           }
           __syncwarp();
-          issued = true;
-          if (++s == PNST_O) { s = 0; ph ^= 1u; }
+          tc_fence_after();
+          for (int r = 0; r < 4 && ok; ++r) {
+            if (!mbar_wait_warp(&bars[PB_FULL + s], ph, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t a0 = pd + (uint64_t)(buf * 2048 + (r & 1) * 1024);
+            const uint64_t b0 = rd + (uint64_t)(s * slot16);
+            const uint32_t d_o = tmem + (uint32_t)((r >> 1) * 256);
+            const uint32_t first = (j > sg.j0 || (r & 1) > 0) ? 1u : 0u;
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc, (first | kk) ? 1u : 0u);
+              mma_commit(&bars[PB_EMPTY + s]);
+            }
+            __syncwarp();
+            issued = true;
+            if (++s == PNST_O) { s = 0; ph ^= 1u; }
+          }
+          if (ok) {
+            if (elect_one()) mma_commit_mc(&bars[PB_PVDONE + buf], (uint16_t)3u);  // both CTAs
+            __syncwarp();
+          }
         }
         if (ok) {
-          if (elect_one()) mma_commit(&bars[PB_PVDONE + buf]);
+          if (elect_one()) mma_commit(&bars[PB_OFINAL]);
           __syncwarp();
         }
-      }
-      if (ok) {
-        if (elect_one()) mma_commit(&bars[PB_OFINAL]);
-        __syncwarp();
+        ++si;
       }
       if (!ok && issued) {
         if (elect_one()) mma_commit(&bars[PB_DRAIN]);
@@ -955,85 +1145,164 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       __syncwarp();
     } else {
       const int q4 = warp & 3;
-      const int row = q4 * 32 + lane;
-      const int query = q0 + row;
-      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-      bool ok = true;
-      if (warp < 6) {
-        // Rescale O rows before P_j V_j when the score CTA raised their
-        // running maximum.
-        const volatile float *alpha_s = reinterpret_cast<const volatile float *>(sm + P_ALPHA);
-        const volatile uint32_t *flags = reinterpret_cast<const volatile uint32_t *>(sm + P_FLAGS);
-        for (int j = 0; j < n; ++j) {
-          const int buf = j % PNPB, u = j / PNPB;
-          if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
-          if (j > 0 && flags[buf * 4 + q4] != 0u) {
-            if (!mbar_wait_warp(&bars[PB_PVDONE + (j - 1) % PNPB], (uint32_t)(((j - 1) / PNPB) & 1), ab)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const float a = alpha_s[buf * 128 + row];
-            for (int cc = 0; cc < 32; ++cc) {
-              uint32_t t[16];
-              tmem_ld16(lane_base + (uint32_t)(cc * 16), t);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * a);
-              tmem_st16(lane_base + (uint32_t)(cc * 16), t);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[PB_OREADY + buf]);
-        }
-      } else if (warp == 6) {
-        // Hand P buffers back to the score CTA as their P V completes.
-        const uint32_t r_pfree0 = mapa_u32(smem_u32(&bars[PB_PFREE]), 0u);
-        if (lane == 0)
-          for (int j = 0; j + PNPB < n; ++j) {
-            if (!mbar_wait(&bars[PB_PVDONE + j % PNPB], (uint32_t)((j / PNPB) & 1), ab)) break;
-            mbar_arrive_remote(r_pfree0 + (uint32_t)((j % PNPB) * 8));
-          }
-        __syncwarp();
-      } else if (warp == 7) {
-        // Hand staging tiles back to the score CTA as their copies land.
-        const uint32_t r_stgfree0 = mapa_u32(smem_u32(&bars[PB_STGFREE]), 0u);
-        if (lane == 0)
-          for (int j = 0; j + 2 < n; ++j) {
-            if (!mbar_wait_cluster(&bars[PB_PFULL + j % PNPB], (uint32_t)((j / PNPB) & 1), ab)) break;
-            mbar_arrive_remote(r_stgfree0 + (uint32_t)((j & 1) * 8));
-          }
-        __syncwarp();
-      }
-      // Epilogue: O / l for this CTA's 128 queries, warps (q4, half) each
-      // writing 16 of the 32 16-column chunks of their rows.  (Warps 6-9 take
-      // no part in the tile loop, so they wait on the one-phase barriers.)
       const int half = (warp - 2) >> 2;
-      if (__all_sync(0xFFFFFFFFu, ok) && mbar_wait_warp(&bars[PB_OFINAL], 0u, ab) &&
-          mbar_wait_cluster_warp(&bars[PB_LFULL], 0u, ab)) {
-        tc_fence_after();
-        const float inv = 1.0f / reinterpret_cast<const volatile float *>(sm + P_LSUM)[row];
-        const int b = bh / args.h, hd = bh % args.h;
-        uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
-        for (int cc = half; cc < 32; cc += 2) {
-          uint32_t t[16];
-          tmem_ld16(lane_base + (uint32_t)(cc * 16), t);
-          tmem_wait_ld();
-          if (query >= args.N) continue;
-          uint4 w0, w1;
-          w0.x = pack_half2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
-          w0.y = pack_half2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
-          w0.z = pack_half2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
-          w0.w = pack_half2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
-          w1.x = pack_half2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
-          w1.y = pack_half2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
-          w1.z = pack_half2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
-          w1.w = pack_half2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
-          reinterpret_cast<uint4 *>(orow + cc * 16)[0] = w0;
-          reinterpret_cast<uint4 *>(orow + cc * 16)[1] = w1;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      const volatile float *alpha_s = reinterpret_cast<const volatile float *>(sm + P_ALPHA);
+      const volatile uint32_t *flags = reinterpret_cast<const volatile uint32_t *>(sm + P_FLAGS);
+      const uint32_t r_lfree = mapa_u32(smem_u32(&bars[PB_LFREE]), 0u);
+      int g = 0, si = 0;
+      PairWalk wk(sp, cid);
+      PairSeg sg;
+      // The eight warps meet at named barriers in every segment, so none
+      // leaves the loop alone: a failed wait is carried to the first barrier
+      // of the segment, which every warp then leaves with the same verdict.
+      while (wk.next(sg)) {
+        if (warp < 6) {
+          // Rescale O rows before P_j V_j when the score CTA raised their
+          // running maximum.
+          for (int j = sg.j0; j < sg.j1 && ok; ++j, ++g) {
+            const int buf = g % PNPB, u = g / PNPB;
+            if (!mbar_wait_cluster_warp(&bars[PB_PFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
+            if (j > sg.j0 && flags[buf * 4 + q4] != 0u) {
+              if (!mbar_wait_warp(&bars[PB_PVDONE + (g - 1) % PNPB], (uint32_t)(((g - 1) / PNPB) & 1), ab)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const float a = alpha_s[buf * 128 + row];
+              for (int cc = 0; cc < 32; ++cc) {
+                uint32_t t[16];
+                tmem_ld16(lane_base + (uint32_t)(cc * 16), t);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * a);
+                tmem_st16(lane_base + (uint32_t)(cc * 16), t);
+              }
+              tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[PB_OREADY + buf]);
+          }
         }
+        // Epilogue of the segment, warps (q4, half) each taking 16 of the 32
+        // 16-column chunks of their rows.
+        const bool eok = ok && mbar_wait_warp(&bars[PB_OFINAL], (uint32_t)(si & 1), ab) &&
+                         mbar_wait_cluster_warp(&bars[PB_LFULL], (uint32_t)(si & 1), ab);
+        float m_row = 0.f, l_row = 1.f;
+        if (eok) {
+          tc_fence_after();
+          m_row = reinterpret_cast<const volatile float *>(sm + P_MROW)[row];
+          l_row = reinterpret_cast<const volatile float *>(sm + P_LSUM)[row];
+        }
+        // All eight warps hold this segment's l and m (or all give up).
+        if (!named_bar_and(1, 256, eok)) {
+          ok = false;
+          break;
+        }
+        if (warp == 2 && lane == 0 && wk.more()) {
+          mbar_arrive_expect_tx(&bars[PB_LFULL], PLM_BYTES);
+          mbar_arrive_remote(r_lfree);
+        }
+        // Warp (q4, half) writes columns half*256 .. +255 of its 32 rows, 32
+        // columns at a time.
+        const int b = sg.bh / args.h, hd = sg.bh % args.h;
+        const int row0 = sg.q0 + q4 * 32;
+        uint16_t *o_w = args.o + ((long long)b * args.N + row0) * args.ldc + (long long)hd * args.d;
+        const int rows_valid = args.N - row0;
+        if (sg.j0 == 0 && sg.j1 == sg.n) {
+          const float inv = 1.0f / l_row;
+          for (int blk = half * 8; blk < half * 8 + 8; ++blk) {
+            uint32_t t[32];
+            tmem_ld32(lane_base + (uint32_t)(blk * 32), t);
+            tmem_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]) * inv;
+            store_o32(o_w, args.ldc, rows_valid, blk * 32, args.d, v, lane);
+          }
+        } else {
+          // Part of a tile cut between clusters: publish this part, count in.
+          // Layout of a part: [16 column blocks][8 pieces][128 rows][4 floats],
+          // so each store (and each load of the merge) moves 512 contiguous
+          // bytes per warp.
+          const int mine = 2 * cid + (sp.ubeg(cid) < sg.cum ? 1 : 0);
+          float *part = args.part + (long long)mine * PART_FLOATS;
+          for (int blk = half * 8; blk < half * 8 + 8; ++blk) {
+            uint32_t t[32];
+            tmem_ld32(lane_base + (uint32_t)(blk * 32), t);
+            tmem_wait_ld();
+#pragma unroll
+            for (int pc = 0; pc < 8; ++pc)
+              __stcg(reinterpret_cast<uint4 *>(part + ((blk * 8 + pc) * 128 + row) * 4),
+                     make_uint4(t[4 * pc], t[4 * pc + 1], t[4 * pc + 2], t[4 * pc + 3]));
+          }
+          if (half == 0) {
+            __stcg(part + PART_O_FLOATS + row, m_row);
+            __stcg(part + PART_O_FLOATS + 128 + row, l_row);
+          }
+          __threadfence();
+          named_bar_sync(1, 256);
+          const int c_lo = sp.owner(sg.cum), c_hi = sp.owner(sg.cum + sg.n - 1);
+          if (warp == 2 && lane == 0) {
+            const uint32_t prev = atomicAdd(args.cnt + sg.t, 1u);
+            *last_flag = prev == (uint32_t)(c_hi - c_lo) ? 1u : 0u;
+          }
+          named_bar_sync(1, 256);
+          if (*last_flag) {
+            // Every other part is published: merge them into this one, each
+            // rescaled to the common row maximum.
+            __threadfence();
+            float M = m_row;
+            for (int c = c_lo; c <= c_hi; ++c)
+              if (c != cid) {
+                const int sl = 2 * c + (sp.ubeg(c) < sg.cum ? 1 : 0);
+                M = fmaxf(M, __ldcg(args.part + (long long)sl * PART_FLOATS + PART_O_FLOATS + row));
+              }
+            const float a_self = exp2f(m_row - M);
+            float L = l_row * a_self;
+            for (int c = c_lo; c <= c_hi; ++c)
+              if (c != cid) {
+                const float *pp = args.part + (long long)(2 * c + (sp.ubeg(c) < sg.cum ? 1 : 0)) * PART_FLOATS;
+                L += __ldcg(pp + PART_O_FLOATS + 128 + row) * exp2f(__ldcg(pp + PART_O_FLOATS + row) - M);
+              }
+            const float inv = 1.0f / L;
+            for (int blk = half * 8; blk < half * 8 + 8; ++blk) {
+              float v[32];
+              {
+                uint32_t t[32];
+                tmem_ld32(lane_base + (uint32_t)(blk * 32), t);
+                tmem_wait_ld();
+                const float as = a_self * inv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]) * as;
+              }
+              for (int c = c_lo; c <= c_hi; ++c)
+                if (c != cid) {
+                  const float *pp = args.part + (long long)(2 * c + (sp.ubeg(c) < sg.cum ? 1 : 0)) * PART_FLOATS;
+                  float4 f[8];
+#pragma unroll
+                  for (int pc = 0; pc < 8; ++pc)
+                    f[pc] = __ldcg(reinterpret_cast<const float4 *>(pp + ((blk * 8 + pc) * 128 + row) * 4));
+                  const float a = exp2f(__ldcg(pp + PART_O_FLOATS + row) - M) * inv;
+#pragma unroll
+                  for (int pc = 0; pc < 8; ++pc) {
+                    v[4 * pc] = fmaf(f[pc].x, a, v[4 * pc]);
+                    v[4 * pc + 1] = fmaf(f[pc].y, a, v[4 * pc + 1]);
+                    v[4 * pc + 2] = fmaf(f[pc].z, a, v[4 * pc + 2]);
+                    v[4 * pc + 3] = fmaf(f[pc].w, a, v[4 * pc + 3]);
+                  }
+                }
+              store_o32(o_w, args.ldc, rows_valid, blk * 32, args.d, v, lane);
+            }
+          }
+        }
+        // O has been read out: the next segment's P V may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[PB_OFREE]);
+        ++si;
       }
     }
   }
@@ -1048,8 +1317,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   }
 }
 
+// Clusters of the pair kernel that are resident at once on the current device.
+int pair_active_clusters(const void *kern) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * PAIR_MAX_CLUSTERS, 1, 1);
+  cfg.blockDim = dim3(PTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    int nsm = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    n = nsm / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
 int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const uint16_t *k, const uint16_t *vt,
-                          cudaStream_t st) {
+                          void *scratch, cudaStream_t st) {
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -1075,18 +1372,43 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  const dim3 grid((dm.N + BQ - 1) / BQ * 2, (unsigned)BH, 1);
   const int var = (a.rel && (a.gw & 31) != 0) ? 2 : ((a.causal || a.rel) ? 1 : 0);
   auto kern = var == 2 ? attention_pair_kernel<2> : (var == 1 ? attention_pair_kernel<1> : attention_pair_kernel<0>);
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-  kern<<<grid, PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
+  const long long nqt = (dm.N + BQ - 1) / BQ, T = (long long)BH * nqt;
+  a.pair_U = a.causal ? (long long)BH * (nqt * (nqt + 1) / 2) : T * nqt;
+  // Splitting tiles pays when whole tiles would leave SM pairs idle.  Under
+  // the causal mask the tiles' lengths differ and heaviest-first whole tiles
+  // already balance well once there are at least as many tiles as SM pairs;
+  // there the split's many short segments (each with its merge) measured
+  // slower, so it is used only for fewer tiles.
+  const int active = scratch ? pair_active_clusters(reinterpret_cast<const void *>(kern)) : 0;
+  if (active > 0 && (!a.causal || T < active)) {
+    a.pair_split = 1;
+    a.pair_P = (int)std::min<long long>(std::min(active, PAIR_MAX_CLUSTERS), a.pair_U);
+    a.part = static_cast<float *>(scratch);
+    a.cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) +
+                                         (size_t)2 * a.pair_P * PART_FLOATS * sizeof(float));
+    if (cudaMemsetAsync(a.cnt, 0, (size_t)T * sizeof(uint32_t), st) != cudaSuccess) return 2;
+  } else {
+    a.pair_split = 0;
+    a.pair_P = (int)T;
+  }
+  kern<<<dim3(2u * (unsigned)a.pair_P, 1, 1), PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
 }  // namespace
 
+size_t attention_scratch_bytes(const Dims &dm) {
+  if (dm.dp != 512) return 0;
+  const long long nqt = (dm.N + BQ - 1) / BQ, T = (long long)dm.B * dm.h * nqt;
+  const long long P = std::min<long long>(PAIR_MAX_CLUSTERS, T * nqt);
+  return (size_t)2 * P * PART_FLOATS * sizeof(float) + (size_t)T * sizeof(uint32_t);
+}
+
 int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
-                     const KParams &kp, cudaStream_t st, int causal, const float *rel) {
+                     const KParams &kp, cudaStream_t st, int causal, const float *rel, void *scratch) {
   AttnArgs a{};
   a.N = dm.N; a.h = dm.h; a.d = dm.d; a.dp = dm.dp; a.ldc = dm.ldc; a.d_o = dm.d_o; a.n_oc = dm.n_oc;
   a.causal = causal; a.rel = rel; a.gh = dm.H; a.gw = dm.W; a.tabn = (2 * dm.H - 1) * (2 * dm.W - 1);
@@ -1098,7 +1420,7 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
     a.err = kp.err;
     a.timeout_ns = kp.timeout_ns;
     a.N = dm.N; a.h = dm.h; a.d = dm.d; a.ldc = dm.ldc;
-    return launch_attention_pair(dm, a, q, k, vt, st);
+    return launch_attention_pair(dm, a, q, k, vt, scratch, st);
   }
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)

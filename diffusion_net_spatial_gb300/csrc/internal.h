@@ -71,7 +71,12 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
 // relative-position table [h][(2H-1)(2W-1)] fp32 (times log2 e) over the
 // dm.H x dm.W token grid.
 int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const uint16_t *vt, uint16_t *o,
-                     const KParams &kp, cudaStream_t st, int causal = 0, const float *rel = nullptr);
+                     const KParams &kp, cudaStream_t st, int causal = 0, const float *rel = nullptr,
+                     void *scratch = nullptr);
+// Scratch the attention step can use to balance its work (head dim 512 only;
+// 0 otherwise): given to launch_attention it lets a query tile be split
+// between SM pairs.  Depends only on the shape.
+size_t attention_scratch_bytes(const Dims &dm);
 
 // Rotary embedding of Q and K in place (q/k layout), token position = row.
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st);

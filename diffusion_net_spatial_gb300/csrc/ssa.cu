@@ -110,7 +110,7 @@ int x_pitch(int N, ssa_dtype dt) {
 
 // Workspace layout of one forward call.
 struct WsLayout {
-  size_t ga, gs, wqkv, bqkv, wo, bo, q, k, vt, o, xpad, rel, total;
+  size_t ga, gs, wqkv, bqkv, wo, bo, q, k, vt, o, xpad, rel, scratch, scratch_bytes, total;
 };
 
 WsLayout ws_layout(const Dims &dm, ssa_dtype dt, bool with_weights, bool with_rel = false) {
@@ -136,6 +136,8 @@ WsLayout ws_layout(const Dims &dm, ssa_dtype dt, bool with_weights, bool with_re
   const int ldx = x_pitch(dm.N, dt);
   if (ldx != dm.N) w.xpad = take((size_t)dm.B * dm.C * ldx * esize(dt));
   if (with_rel) w.rel = take((size_t)dm.h * (2 * dm.H - 1) * (2 * dm.W - 1) * 4);
+  w.scratch_bytes = attention_scratch_bytes(dm);
+  if (w.scratch_bytes) w.scratch = take(w.scratch_bytes);
   w.total = off;
   return w;
 }
@@ -214,7 +216,7 @@ ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, con
     e = launch_rel_table_pack((int)dt, var.rel_table, dm.H, dm.W, dm.h, rel, st);
     if (e != cudaSuccess) return cuda_fail(e, "rel table pack launch");
   }
-  r = launch_attention(dm, q, k, vt, o, kp, st, var.causal, rel);
+  r = launch_attention(dm, q, k, vt, o, kp, st, var.causal, rel, wl.scratch_bytes ? ws + wl.scratch : nullptr);
   if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "attention launch");
   r = launch_out_proj(dm, (int)dt, o, w_o, b_o, x, out, kp, st);

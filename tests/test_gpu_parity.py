@@ -68,7 +68,10 @@ SMALL = [
     # name, B, C, H, W, G, h, dtype
     ("ragged-d64", 2, 128, 12, 20, 8, 2, "f32"),       # N = 240: one full 128 tile + ragged tail
     ("ragged-d40", 1, 80, 9, 15, 8, 2, "f32"),         # d = 40 -> padded to 48; N = 135
-    ("ragged-d512", 1, 512, 10, 13, 32, 1, "f32"),     # d = 512: two 256-wide output halves; N = 130
+    ("ragged-d512", 1, 512, 10, 13, 32, 1, "f32"),     # d = 512 (score + output CTA pairs); N = 130
+    ("d512-split3", 2, 512, 16, 24, 32, 1, "f32"),     # N = 384: every query tile shared by three SM pairs
+    ("d496", 1, 496, 10, 13, 16, 1, "f32"),            # d = 496 padded to 512: the last 16 columns unwritten
+    ("d500-b2", 2, 500, 9, 14, 20, 1, "f32"),          # d = 500 (not a multiple of 8): element stores
     ("d16-multihead", 2, 64, 5, 7, 4, 4, "f32"),       # N = 35 (not a multiple of 4: padded-x path)
     ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
     ("single-pixel", 3, 64, 1, 1, 64, 2, "f32"),       # H = W = 1, one channel per group
