@@ -314,6 +314,9 @@ def run_ours(args, rank, world, local):
         pk = ssa.ssa_pack_weights(pd, wl.num_heads, stream=stream)
     names = ["gn_stats", "qkv_gemm", "attention", "out_proj"]
     per = {n: [] for n in names}
+    # the attention step with the same scratch the planned forward gives it
+    ws_att_bytes = ssa.attention_workspace_size(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
+    ws_att = torch.empty(ws_att_bytes, dtype=torch.uint8, device=dev) if ws_att_bytes else None
     kb = max(3, min(K, 20))
     with torch.cuda.stream(stream):
         for i in range(kb + 2):
@@ -325,7 +328,7 @@ def run_ours(args, rank, world, local):
             ev[1].record(stream)
             q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], wl.num_heads, stream=stream)
             ev[2].record(stream)
-            o = ssa.ssa_attention(q, k, vt, wl.B, wl.C, wl.N, wl.num_heads, stream=stream)
+            o = ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads, stream=stream, workspace=ws_att)
             ev[3].record(stream)
             ssa.ssa_out_project(o, pk["w_o"], pk["b_o"], xd, out=out, stream=stream)
             ev[4].record(stream)

@@ -29,7 +29,9 @@ EXPORTS = ("ssa_workspace_size", "ssa_forward", "ssa_plan_create", "ssa_plan_wor
            "ssa_qkv_project", "ssa_attention", "ssa_out_project", "ssa_get_device_status",
            "ssa_set_wait_timeout_ns", "ssa_debug_timeout_probe", "ssa_last_error_string",
            "ssa_launches_per_forward", "ssa_workspace_size_ex", "ssa_forward_ex", "ssa_plan_workspace_size_ex",
-           "ssa_forward_planned_ex", "ssa_rope", "ssa_qk_norm", "ssa_pack_rel_table", "ssa_attention_ex")
+           "ssa_forward_planned_ex", "ssa_rope", "ssa_qk_norm", "ssa_pack_rel_table", "ssa_attention_ex",
+           "ssa_attention_workspace_size", "ssa_attention_ws", "ssa_set_attention_split")
+SPLIT_AUTO, SPLIT_ALWAYS, SPLIT_NEVER = 0, 1, 2
 BIAS_KEYS = ("q_bias", "k_bias", "v_bias", "out_bias")
 
 
@@ -82,6 +84,9 @@ def load_library():
         "ssa_qk_norm": ([vp, vp, i32, i32, i32, i32, i32, vp, vp, vp], i32),
         "ssa_pack_rel_table": ([vp, i32, i32, i32, i32, vp, vp], i32),
         "ssa_attention_ex": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp], i32),
+        "ssa_attention_workspace_size": ([i32] * 5, sz),
+        "ssa_attention_ws": ([vp, vp, vp] + [i32] * 6 + [vp, vp, vp, sz, vp], i32),
+        "ssa_set_attention_split": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -343,16 +348,33 @@ def ssa_pack_rel_table(table: torch.Tensor, H: int, W: int, num_heads: int, stre
 
 
 def ssa_attention_ex(q, k, vt, B: int, C: int, H: int, W: int, num_heads: int, causal=False, rel_packed=None,
-                     o=None, stream=None):
+                     o=None, stream=None, workspace=None):
     """ssa_attention over the H x W token grid with the causal mask and the
-    packed relative-position table (ssa_pack_rel_table)."""
+    packed relative-position table (ssa_pack_rel_table).  With `workspace`
+    (a uint8 device tensor of at least attention_workspace_size bytes, 256-byte
+    aligned) a head dim of 512 may split query tiles between SM pairs
+    (ssa_attention_ws)."""
     lib = load_library()
     lay = layout(B, C, H, W, num_heads)
     if o is None:
         o = torch.empty(B, H * W, lay["ldc"], dtype=torch.float16, device=q.device)
-    _check(lib.ssa_attention_ex(_ptr(q), _ptr(k), _ptr(vt), B, C, H, W, num_heads, int(bool(causal)),
-                                _ptr(rel_packed), _ptr(o), _stream(stream)))
+    if workspace is None:
+        _check(lib.ssa_attention_ex(_ptr(q), _ptr(k), _ptr(vt), B, C, H, W, num_heads, int(bool(causal)),
+                                    _ptr(rel_packed), _ptr(o), _stream(stream)))
+    else:
+        _check(lib.ssa_attention_ws(_ptr(q), _ptr(k), _ptr(vt), B, C, H, W, num_heads, int(bool(causal)),
+                                    _ptr(rel_packed), _ptr(o), _ptr(workspace), workspace.numel(), _stream(stream)))
     return o
+
+
+def attention_workspace_size(B: int, C: int, H: int, W: int, num_heads: int) -> int:
+    """Bytes of scratch ssa_attention_ws can use for this shape (0: none)."""
+    return int(load_library().ssa_attention_workspace_size(B, C, H, W, num_heads))
+
+
+def set_attention_split(policy: int):
+    """SPLIT_AUTO, SPLIT_ALWAYS or SPLIT_NEVER (ssa_set_attention_split)."""
+    _check(load_library().ssa_set_attention_split(int(policy)))
 
 
 def ssa_out_project(o, w_o, b_o, x: torch.Tensor, out=None, stream=None):

@@ -1377,13 +1377,16 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   const long long nqt = (dm.N + BQ - 1) / BQ, T = (long long)BH * nqt;
   a.pair_U = a.causal ? (long long)BH * (nqt * (nqt + 1) / 2) : T * nqt;
-  // Splitting tiles pays when whole tiles would leave SM pairs idle.  Under
-  // the causal mask the tiles' lengths differ and heaviest-first whole tiles
-  // already balance well once there are at least as many tiles as SM pairs;
-  // there the split's many short segments (each with its merge) measured
-  // slower, so it is used only for fewer tiles.
-  const int active = scratch ? pair_active_clusters(reinterpret_cast<const void *>(kern)) : 0;
-  if (active > 0 && (!a.causal || T < active)) {
+  // By default tiles are split only when there are more tiles than clusters
+  // (a partial last wave; every piece then spans at least one tile, so a tile
+  // has at most two contributors).  With fewer tiles the pieces shrink to a
+  // few key tiles and the parts and merges cost more than the idle SM pairs
+  // (vae1024: 69 vs 34 us); under the causal mask heaviest-first whole tiles
+  // measured faster (273-281 vs 367-378 us at 128 tiles).
+  const int policy = attention_split_policy();
+  const int active =
+      (scratch && policy != 2) ? pair_active_clusters(reinterpret_cast<const void *>(kern)) : 0;
+  if (active > 0 && (policy == 1 || (!a.causal && T > active))) {
     a.pair_split = 1;
     a.pair_P = (int)std::min<long long>(std::min(active, PAIR_MAX_CLUSTERS), a.pair_U);
     a.part = static_cast<float *>(scratch);

@@ -77,6 +77,9 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
 // 0 otherwise): given to launch_attention it lets a query tile be split
 // between SM pairs.  Depends only on the shape.
 size_t attention_scratch_bytes(const Dims &dm);
+// Policy for using that scratch (ssa_set_attention_split): 0 auto, 1 always,
+// 2 never.
+int attention_split_policy();
 
 // Rotary embedding of Q and K in place (q/k layout), token position = row.
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st);

@@ -26,6 +26,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 thread_local char t_err[512] = "";
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_split_policy{0};
 std::mutex g_mu;
 uint32_t *g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
@@ -65,6 +66,12 @@ ssa_status device_state(uint32_t **err, int *num_sms) {
   if (num_sms) *num_sms = g_num_sms[dev];
   return SSA_OK;
 }
+
+}  // namespace
+
+int attention_split_policy() { return g_split_policy.load(); }
+
+namespace {
 
 ssa_status kparams(KParams *kp, int *num_sms) {
   uint32_t *err = nullptr;
@@ -280,6 +287,18 @@ extern "C" {
 const char *ssa_last_error_string(void) { return t_err; }
 
 void ssa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+ssa_status ssa_set_attention_split(int policy) {
+  if (policy < SSA_SPLIT_AUTO || policy > SSA_SPLIT_NEVER)
+    return fail(SSA_ERR_CONSTRAINT, "split policy %d is not SSA_SPLIT_AUTO, _ALWAYS or _NEVER", policy);
+  g_split_policy.store(policy);
+  return SSA_OK;
+}
+
+size_t ssa_attention_workspace_size(int B, int C, int H, int W, int num_heads) {
+  if (num_heads <= 0 || check_shape(B, C, H, W, 0, num_heads) != SSA_OK) return 0;
+  return attention_scratch_bytes(make_dims(B, C, H, W, 1, num_heads));
+}
 
 int ssa_launches_per_forward(int planned) { return planned ? 4 : 5; }
 
@@ -578,6 +597,31 @@ ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t
   if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
   const Dims dm = make_dims(B, C, H, W, 1, num_heads);
   const int r = launch_attention(dm, q, k, vt, o, kp, static_cast<cudaStream_t>(stream), causal ? 1 : 0, rel_packed);
+  if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
+  if (r) return cuda_fail(cudaGetLastError(), "attention launch");
+  return SSA_OK;
+}
+
+ssa_status ssa_attention_ws(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int B, int C, int H, int W,
+                            int num_heads, int causal, const float *rel_packed, uint16_t *o, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
+  ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s != SSA_OK) return s;
+  if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
+    return fail(SSA_ERR_ALIGNMENT, "q, k, vt and o must be 16-byte aligned");
+  const Dims dm = make_dims(B, C, H, W, 1, num_heads);
+  const size_t need = attention_scratch_bytes(dm);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SSA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (workspace && workspace_bytes < need)
+    return fail(SSA_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  KParams kp{};
+  int num_sms = 0;
+  if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
+  const int r = launch_attention(dm, q, k, vt, o, kp, static_cast<cudaStream_t>(stream), causal ? 1 : 0, rel_packed,
+                                 (workspace && need) ? workspace : nullptr);
   if (r == 1) return fail(SSA_ERR_CUDA, "attention: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "attention launch");
   return SSA_OK;

@@ -245,6 +245,34 @@ ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t
                             int B, int C, int H, int W, int num_heads, int causal,
                             const float *rel_packed, uint16_t *o, void *stream);
 
+/* Head dimension 512 (padded) runs as two-CTA clusters, one per resident SM
+ * pair.  With scratch, the (query tile, key tile) work of a call can be cut
+ * into equal pieces, one per cluster, so no SM pair idles in a partial last
+ * wave; a query tile shared by several clusters is finished by its last
+ * contributor, which merges the others' fp32 parts (each rescaled to the
+ * common row maximum, as in the online softmax) -- the result equals the
+ * unsplit one up to rounding.
+ *
+ * ssa_attention_workspace_size: bytes of that scratch for this shape (0 when
+ *   the head dim is not padded to 512, or the shape is invalid).  The
+ *   ssa_forward* workspaces already include it.
+ * ssa_attention_ws: ssa_attention_ex with that scratch: `workspace` (device,
+ *   256-byte aligned, >= the size above, caller-owned, contents ignored) or
+ *   NULL to run whole query tiles.  SSA_ERR_WORKSPACE when too small.
+ * ssa_set_attention_split: when the scratch is used -- SSA_SPLIT_AUTO (when
+ *   there are more query tiles than resident clusters and no causal mask:
+ *   measured to pay there), SSA_SPLIT_ALWAYS, SSA_SPLIT_NEVER.  Process-wide,
+ *   for launches after the call; SSA_ERR_CONSTRAINT for another value. */
+#define SSA_SPLIT_AUTO 0
+#define SSA_SPLIT_ALWAYS 1
+#define SSA_SPLIT_NEVER 2
+size_t ssa_attention_workspace_size(int B, int C, int H, int W, int num_heads);
+ssa_status ssa_attention_ws(const uint16_t *q, const uint16_t *k, const uint16_t *vt,
+                            int B, int C, int H, int W, int num_heads, int causal,
+                            const float *rel_packed, uint16_t *o, void *workspace,
+                            size_t workspace_bytes, void *stream);
+ssa_status ssa_set_attention_split(int policy);
+
 /* --------------------------------------------------------- diagnostics --- */
 
 /* Synchronises `stream`, then reads and clears the device error flag:

@@ -96,3 +96,16 @@ def test_bad_shapes_rejected_without_device(lib):
 def test_launch_count(lib):
     assert ssa.ssa_launches_per_forward(False) == 5
     assert ssa.ssa_launches_per_forward(True) == 4
+
+
+def test_attention_scratch_size_and_split_policy(lib):
+    # head dim 512: two parts of 128 x 512 fp32 + 256 row values per cluster
+    # (at most 76 clusters) and one counter per query tile; other head dims: none
+    nqt = (128 * 128 + 127) // 128
+    assert ssa.attention_workspace_size(1, 512, 128, 128, 1) == 2 * 76 * (128 * 512 + 256) * 4 + nqt * 4
+    assert ssa.attention_workspace_size(1, 512, 4, 4, 1) == 2 * 1 * (128 * 512 + 256) * 4 + 4  # one unit
+    assert ssa.attention_workspace_size(2, 320, 64, 64, 8) == 0
+    assert ssa.attention_workspace_size(1, 64, 0, 8, 2) == 0
+    assert lib.ssa_set_attention_split(7) == 1
+    for p in (ssa.SPLIT_ALWAYS, ssa.SPLIT_NEVER, ssa.SPLIT_AUTO):
+        assert lib.ssa_set_attention_split(p) == 0

@@ -219,3 +219,75 @@ def test_argument_errors(ssa):
     with pytest.raises(ssa.SsaError) as e:
         ssa.ssa_forward(xd.double(), {k: v.double() for k, v in pd.items()}, 8, 2)
     assert e.value.status == 2
+
+
+# ---------------------------------------------------------------------------
+# Head dim 512: query tiles split between SM pairs (ssa_set_attention_split).
+# The split merges fp32 parts rescaled to a common row maximum, which equals
+# the unsplit online softmax up to rounding; both schedules are checked
+# against the oracle on shapes where every query tile is shared by several
+# clusters (ALWAYS) and where none is (NEVER).
+
+@pytest.fixture
+def split_policy(ssa):
+    yield
+    ssa.set_attention_split(ssa.SPLIT_AUTO)
+
+
+SPLIT_CASES = [
+    # name, B, C, H, W, G, h
+    ("n300", 1, 512, 12, 25, 32, 1),     # 3 query tiles x 3 key tiles, ragged last tile
+    ("b2-n384", 2, 512, 16, 24, 32, 1),  # 6 query tiles over 2 samples
+    ("d496", 1, 496, 10, 13, 16, 1),     # padded head dim, 2 query tiles
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+@pytest.mark.parametrize("policy", ["always", "never"])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_pair_split_policies(ssa, split_policy, case, policy, causal):
+    name, B, C, H, W, G, h = case
+    ssa.set_attention_split(ssa.SPLIT_ALWAYS if policy == "always" else ssa.SPLIT_NEVER)
+    wl = wls.custom(name, B, C, H, W, G, h, "f32", seed=21)
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    out = ssa.ssa_forward(xd, pd, G, h, causal=causal)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    ref, y = oracle.block(x, p, G, h, causal=causal)
+    got = out.double().cpu().numpy().reshape(B, C, -1)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(y), 1e-30)
+    mx = np.abs(got - ref).max()
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_pair_split_matches_whole_tiles(ssa, split_policy):
+    """The split and the whole-tile schedules agree to rounding on the same
+    inputs, and the attention step with scratch equals the planned block's."""
+    wl = wls.custom("split-eq", 1, 512, 16, 32, 32, 1, "f32", seed=22)  # 4 query tiles x 4 key tiles
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    ssa.set_attention_split(ssa.SPLIT_ALWAYS)
+    a = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads)
+    ssa.set_attention_split(ssa.SPLIT_NEVER)
+    b = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads)
+    assert ssa.ssa_get_device_status() == 0
+    d = (a.double() - b.double()).abs().max().item()
+    assert d <= 2e-3, d
+    # step API with and without scratch
+    _, _, ga, gs = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, wl.num_heads)
+    q, k, vt = ssa.ssa_qkv_project(xd, ga, gs, pk["w_qkv"], pk["b_qkv"], wl.num_heads)
+    nbytes = ssa.attention_workspace_size(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ssa.set_attention_split(ssa.SPLIT_ALWAYS)
+    o1 = ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads, workspace=ws)
+    o2 = ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads)
+    assert ssa.ssa_get_device_status() == 0
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-3
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads, workspace=ws[: nbytes // 2])
+    assert e.value.status == 5
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.set_attention_split(7)
+    assert e.value.status == 1
