@@ -93,10 +93,39 @@ __host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot, int p
 //    score becomes the base-2 logit s * log2(e)/sqrt(d) + table[dy, dx].
 //    When W is a multiple of 32, a warp's queries share one grid row and each
 //    32-key chunk lies in one grid row, so the 32 x 32 bias block is a
-//    Toeplitz slice of one table row: 63 consecutive entries, loaded once per
-//    warp (two per lane) and handed out with one shuffle per score.  Other
-//    widths read the table per score.
+//    Toeplitz slice of one table row: the entry of lane l and key i is
+//    p[-i] for a per-lane pointer p, one L1-resident load at a constant
+//    offset per score (the rows of the next key tile are prefetched into L1
+//    a tile ahead, rel_prefetch).  Other widths read the table per score with
+//    full index arithmetic.
 // Returns true when the scores were turned into base-2 logits.
+
+// Pointer p of the chunk of keys kc .. kc+31 (one grid row) for this lane's
+// query of the warp whose first query is qw (W % 32 == 0).
+__device__ __forceinline__ const float *rel_row_ptr(const AttnArgs &args, const float *tab, int qw, int kc,
+                                                    int lane) {
+  const int gw = args.gw, row_len = 2 * gw - 1;
+  const int rq = qw / gw, cq0 = qw - rq * gw;
+  const int rk = kc / gw, ck0 = kc - rk * gw;
+  return tab + (rq - rk + args.gh - 1) * row_len + (cq0 - ck0 + gw - 1) + lane;
+}
+
+// Brings the table entries of NC chunks of keys from k0 into L1 (W % 32 == 0).
+template <int NC>
+__device__ __forceinline__ void rel_prefetch(const AttnArgs &args, int head, int query, int k0, int lane) {
+  const int qw = query - lane;
+  if (args.rel == nullptr || qw >= args.N) return;
+  const float *tab = args.rel + (long long)head * args.tabn;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int kc = k0 + 32 * c;
+    if (kc >= args.N) continue;
+    const float *p = rel_row_ptr(args, tab, qw, kc, lane);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p - 31));
+  }
+}
+
 template <int NC, bool GENERIC>
 __device__ __forceinline__ bool apply_variants(uint32_t (&r)[NC][32], const AttnArgs &args, int head, int query,
                                                int k0, float sl2, int lane) {
@@ -115,7 +144,6 @@ __device__ __forceinline__ bool apply_variants(uint32_t (&r)[NC][32], const Attn
   const int qw = query - lane;  // the warp's first query
   if (!GENERIC) {  // W % 32 == 0 (checked at launch)
     if (qw < args.N) {  // warp-uniform: N is a multiple of 32 here
-      const int rq = qw / gw, cq0 = qw - rq * gw;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const int kc = k0 + 32 * c;
@@ -124,26 +152,9 @@ __device__ __forceinline__ bool apply_variants(uint32_t (&r)[NC][32], const Attn
           for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(-INFINITY);
           continue;
         }
-        const int rk = kc / gw, ck0 = kc - rk * gw;
-        // entry for (lane l, key i): e0 + l - i with e0 the lane-0, key-0 entry
-        const int e0 = (rq - rk + args.gh - 1) * row_len + (cq0 - ck0 + gw - 1);
-        // An opaque copy of the lane index: the per-step lane arithmetic below
-        // is then recomputed per chunk instead of being held in 64 registers
-        // across all chunks.
-        int ln = lane;
-        asm volatile("" : "+r"(ln));
-        const float w0 = __ldg(tab + e0 - 31 + ln);             // window entries 0 .. 31
-        const float w1 = ln < 31 ? __ldg(tab + e0 + 1 + ln) : 0.f;  // window entries 32 .. 62
+        const float *p = rel_row_ptr(args, tab, qw, kc, lane);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          // Lane l needs window entry l - i + 31: from lane (l + 31 - i) % 32,
-          // register w0 when l <= i, else w1.  The sending lane knows its one
-          // receiver (lane + i + 1) % 32, so it picks the register: one
-          // shuffle per score.
-          const int recv = (ln + i + 1) & 31;
-          const float b = __shfl_sync(0xFFFFFFFFu, recv <= i ? w0 : w1, (ln + 31 - i) & 31);
-          r[c][i] = __float_as_uint(fmaf(__uint_as_float(r[c][i]), sl2, b));
-        }
+        for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(fmaf(__uint_as_float(r[c][i]), sl2, __ldg(p - i)));
       }
     } else {
 #pragma unroll
@@ -411,6 +422,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     constexpr bool var = VAR != 0;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    if (VAR == 1) rel_prefetch<4>(args, bh % args.h, query, 0, lane);
     for (int j = 0; j < n; ++j) {
       const int buf = single ? 0 : (j & 1);
       const uint32_t par = single ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
@@ -436,6 +448,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       }
       float sc = sl2;  // base-2 logits when the table was added
       if (var && apply_variants<4, VAR == 2>(r, args, bh % args.h, query, j * BKV, sl2, lane)) sc = 1.f;
+      if (VAR == 1 && j + 1 < n) rel_prefetch<4>(args, bh % args.h, query, (j + 1) * BKV, lane);
       // Row maximum: eight independent 3-input max chains.
       float pm[8];
 #pragma unroll
@@ -957,6 +970,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           if (lane == 0) mbar_arrive(&bars[PB_QREADY]);
         }
         float m_used = -INFINITY, l = 0.f;
+        if (VAR == 1) rel_prefetch<2>(args, bh % args.h, q0 + row, ((sg.j0 + sg.rot) % sg.n) * PK + half * 64, lane);
         for (int j = sg.j0; j < sg.j1; ++j, ++g, ++xi) {
           const int buf = g & 1, u = g >> 1;
           if (!mbar_wait_warp(&bars[PB_SFULL + buf], (uint32_t)(u & 1), ab)) { ok = false; break; }
@@ -980,6 +994,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           float sc = sl2;  // base-2 logits when the table was added
           if (var && apply_variants<2, VAR == 2>(r, args, bh % args.h, q0 + row, kt * PK + half * 64, sl2, lane))
             sc = 1.f;
+          if (VAR == 1 && j + 1 < sg.j1)
+            rel_prefetch<2>(args, bh % args.h, q0 + row, ((j + 1 + sg.rot) % sg.n) * PK + half * 64, lane);
           float pm[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
