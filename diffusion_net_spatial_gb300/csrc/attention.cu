@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
   const uint32_t TM_O = (uint32_t)args.o_col;
 
@@ -832,6 +834,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
   const uint32_t slot16 = (uint32_t)PSLOT >> 4;
   bool ok = true;
@@ -1413,7 +1417,7 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
     a.pair_split = 0;
     a.pair_P = (int)T;
   }
-  kern<<<dim3(2u * (unsigned)a.pair_P, 1, 1), PTHREADS, P_SMEM, st>>>(kmap, vmap, a);
+  (void)launch_k(kern, dim3(2u * (unsigned)a.pair_P, 1, 1), dim3(PTHREADS), P_SMEM, st, kmap, vmap, a);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
@@ -1507,12 +1511,12 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   if (a.single) {
     auto kern = var == 2 ? attention_kernel<true, 2> : (var == 1 ? attention_kernel<true, 1> : attention_kernel<true, 0>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+    (void)launch_k(kern, dim3(grid), dim3(THREADS), smem, st, qmap, kmap, vmap, a);
   } else {
     auto kern =
         var == 2 ? attention_kernel<false, 2> : (var == 1 ? attention_kernel<false, 1> : attention_kernel<false, 0>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, THREADS, smem, st>>>(qmap, kmap, vmap, a);
+    (void)launch_k(kern, dim3(grid), dim3(THREADS), smem, st, qmap, kmap, vmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) gn_stats_kernel(const void *__restri
                                                             float *rstd, float *ga, float *gs) {
   constexpr int VW = DT == 0 ? 4 : 8;  // elements per 16-byte vector
   constexpr int UNROLL = 4;
+  pdl_trigger();
+  pdl_wait();
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
   const int cs = (int)cl.num_blocks();
@@ -216,13 +218,15 @@ cudaError_t launch_gn_stats(const void *x, int B, int C, int N, int G, int dtype
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (dtype == 0)
     return cudaLaunchKernelEx(&cfg, gn_stats_kernel<0>, x, C, N, G, gw, gb, mean, rstd, a, s);
   return cudaLaunchKernelEx(&cfg, gn_stats_kernel<1>, x, C, N, G, gw, gb, mean, rstd, a, s);

@@ -49,6 +49,32 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const 
                       const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                       CUtensorMapSwizzle swz);
 
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the
+// stream be scheduled (its CTAs then wait in pdl_wait); pdl_wait blocks until
+// the previous kernel of the stream has completed and its memory is visible
+// (it returns at once when the launch had no programmatic dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kern` with programmatic dependent launch allowed: its CTAs may be
+// scheduled while the previous kernel of the stream still runs; every kernel
+// of this library waits (pdl_wait) before its first global memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---- launch wrappers (each returns the launch error, if any) ----
 cudaError_t launch_gn_stats(const void *x, int B, int C, int N, int G, int dtype, const void *gw,
                             const void *gb, float *mean, float *rstd, float *a, float *s, int num_sms,

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
 
   if (warp == 0) {
@@ -337,6 +339,8 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
 
   if (warp == 0 || warp == 10) {
@@ -544,10 +548,10 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
     const dim3 grid((dm.N + BM - 1) / BM, dm.B, 1);
     if (dtype == 0) {
       cudaFuncSetAttribute(out_proj_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      out_proj_resident_kernel<0><<<grid, ORTHREADS, smem, st>>>(omap, wres, xres, outres, r);
+      (void)launch_k(out_proj_resident_kernel<0>, dim3(grid), dim3(ORTHREADS), smem, st, omap, wres, xres, outres, r);
     } else {
       cudaFuncSetAttribute(out_proj_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      out_proj_resident_kernel<1><<<grid, ORTHREADS, smem, st>>>(omap, wres, xres, outres, r);
+      (void)launch_k(out_proj_resident_kernel<1>, dim3(grid), dim3(ORTHREADS), smem, st, omap, wres, xres, outres, r);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
@@ -560,10 +564,10 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
   const dim3 grid((dm.C + BN - 1) / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(out_proj_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    out_proj_kernel<0><<<grid, THREADS, smem, st>>>(omap, wmap, xmap, outmap, a);
+    (void)launch_k(out_proj_kernel<0>, dim3(grid), dim3(THREADS), smem, st, omap, wmap, xmap, outmap, a);
   } else {
     cudaFuncSetAttribute(out_proj_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    out_proj_kernel<1><<<grid, THREADS, smem, st>>>(omap, wmap, xmap, outmap, a);
+    (void)launch_k(out_proj_kernel<1>, dim3(grid), dim3(THREADS), smem, st, omap, wmap, xmap, outmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

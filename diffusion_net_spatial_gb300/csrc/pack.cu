@@ -31,6 +31,8 @@ template <int DT>
 __global__ void pack_kernel(int C, int h, int d, int dp, int ldc, const void *wq, const void *bq,
                             const void *wk, const void *bk, const void *wv, const void *bv, const void *wo,
                             const void *bo, uint16_t *w_qkv, float *b_qkv, uint16_t *w_o, float *b_o) {
+  pdl_trigger();
+  pdl_wait();
   const long long n_qkv = 3LL * h * dp * ldc;
   const long long n_o = (long long)C * ldc;
   const long long total = n_qkv + n_o;
@@ -67,6 +69,8 @@ __global__ void pack_kernel(int C, int h, int d, int dp, int ldc, const void *wq
 }
 
 __global__ void pad_x_kernel(const char *x, int rows, int n_bytes, int ld_bytes, char *dst) {
+  pdl_trigger();
+  pdl_wait();
   const long long total = (long long)rows * ld_bytes;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -87,10 +91,10 @@ cudaError_t launch_pack_weights(const Dims &dm, int dtype, const void *wq, const
   const long long blocks = (total + threads - 1) / threads;
   const int grid = (int)(blocks < 4096 ? blocks : 4096);
   if (dtype == 0)
-    pack_kernel<0><<<grid, threads, 0, st>>>(dm.C, dm.h, dm.d, dm.dp, dm.ldc, wq, bq, wk, bk, wv, bv, wo, bo,
+    (void)launch_k(pack_kernel<0>, dim3(grid), dim3(threads), 0, st, dm.C, dm.h, dm.d, dm.dp, dm.ldc, wq, bq, wk, bk, wv, bv, wo, bo,
                                              w_qkv, b_qkv, w_o, b_o);
   else
-    pack_kernel<1><<<grid, threads, 0, st>>>(dm.C, dm.h, dm.d, dm.dp, dm.ldc, wq, bq, wk, bk, wv, bv, wo, bo,
+    (void)launch_k(pack_kernel<1>, dim3(grid), dim3(threads), 0, st, dm.C, dm.h, dm.d, dm.dp, dm.ldc, wq, bq, wk, bk, wv, bv, wo, bo,
                                              w_qkv, b_qkv, w_o, b_o);
   return cudaGetLastError();
 }
@@ -100,7 +104,7 @@ cudaError_t launch_pad_x(const void *x, int B, int C, int N, int ldx, int esize,
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   const int grid = (int)(blocks < 4096 ? blocks : 4096);
-  pad_x_kernel<<<grid, threads, 0, st>>>(reinterpret_cast<const char *>(x), B * C, N * esize, ldx * esize,
+  (void)launch_k(pad_x_kernel, dim3(grid), dim3(threads), 0, st, reinterpret_cast<const char *>(x), B * C, N * esize, ldx * esize,
                                          reinterpret_cast<char *>(dst));
   return cudaGetLastError();
 }

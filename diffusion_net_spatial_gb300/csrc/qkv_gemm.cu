@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
 
   if (warp == 0) {
@@ -395,6 +397,8 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
   const Abort ab{abort_flag, args.err, args.timeout_ns};
 
   if (warp == 0 || warp == 10) {
@@ -699,10 +703,10 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     const dim3 grid(ng, (dm.N + BM - 1) / BM, dm.B);
     if (dtype == 0) {
       cudaFuncSetAttribute(qkv_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      qkv_resident_kernel<0><<<grid, RTHREADS, smem, st>>>(xmap, wmap, r);
+      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap, r);
     } else {
       cudaFuncSetAttribute(qkv_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      qkv_resident_kernel<1><<<grid, RTHREADS, smem, st>>>(xmap, wmap, r);
+      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap, r);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
@@ -717,10 +721,10 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
   const dim3 grid(dm.ntot / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(qkv_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_gemm_kernel<0><<<grid, THREADS, smem, st>>>(xmap, wmap, qmap, kmap, vmap, a);
+    (void)launch_k(qkv_gemm_kernel<0>, dim3(grid), dim3(THREADS), smem, st, xmap, wmap, qmap, kmap, vmap, a);
   } else {
     cudaFuncSetAttribute(qkv_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_gemm_kernel<1><<<grid, THREADS, smem, st>>>(xmap, wmap, qmap, kmap, vmap, a);
+    (void)launch_k(qkv_gemm_kernel<1>, dim3(grid), dim3(THREADS), smem, st, xmap, wmap, qmap, kmap, vmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

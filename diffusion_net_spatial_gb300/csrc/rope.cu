@@ -26,6 +26,8 @@ namespace ssa {
 namespace {
 
 __global__ void rope_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int ldq, int d) {
+  pdl_trigger();
+  pdl_wait();
   const int hd = d / 2;
   const long long total = rows * hd;
   const float l2base = -2.0f * 13.287712379549449f / (float)d;  // -2 log2(10000) / d
@@ -59,6 +61,8 @@ __device__ __forceinline__ float ld_x(const void *p, long long i) {
 template <int DT>
 __global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int h, int ldq, int d,
                                const void *qg, const void *kg) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   const float sd = sqrtf((float)d);
@@ -83,6 +87,8 @@ __global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, long long rows, int N, 
 
 template <int DT>
 __global__ void rel_table_pack_kernel(const void *table, int entries, int heads, float *packed) {
+  pdl_trigger();
+  pdl_wait();
   const long long total = (long long)entries * heads;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -110,7 +116,7 @@ int grid_for(long long work) {
 
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st) {
   const long long rows = (long long)dm.B * dm.h * dm.N;
-  rope_kernel<<<grid_for(rows * (dm.d / 2)), 256, 0, st>>>(q, k, rows, dm.N, dm.ldq, dm.d);
+  (void)launch_k(rope_kernel, dim3(grid_for(rows * (dm.d / 2))), dim3(256), 0, st, q, k, rows, dm.N, dm.ldq, dm.d);
   return cudaGetLastError();
 }
 
@@ -120,9 +126,9 @@ cudaError_t launch_qk_norm(const Dims &dm, int dtype, uint16_t *q, uint16_t *k, 
   long long blocks = (2 * rows + 7) / 8;  // 8 warps (rows) per block
   if (blocks > 8192) blocks = 8192;
   if (dtype == 0)
-    qk_norm_kernel<0><<<(int)blocks, 256, 0, st>>>(q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
+    (void)launch_k(qk_norm_kernel<0>, dim3((int)blocks), dim3(256), 0, st, q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
   else
-    qk_norm_kernel<1><<<(int)blocks, 256, 0, st>>>(q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
+    (void)launch_k(qk_norm_kernel<1>, dim3((int)blocks), dim3(256), 0, st, q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
   return cudaGetLastError();
 }
 
@@ -130,9 +136,9 @@ cudaError_t launch_rel_table_pack(int dtype, const void *table, int H, int W, in
                                   cudaStream_t st) {
   const int entries = (2 * H - 1) * (2 * W - 1);
   if (dtype == 0)
-    rel_table_pack_kernel<0><<<grid_for((long long)entries * heads), 256, 0, st>>>(table, entries, heads, packed);
+    (void)launch_k(rel_table_pack_kernel<0>, dim3(grid_for((long long)entries * heads)), dim3(256), 0, st, table, entries, heads, packed);
   else
-    rel_table_pack_kernel<1><<<grid_for((long long)entries * heads), 256, 0, st>>>(table, entries, heads, packed);
+    (void)launch_k(rel_table_pack_kernel<1>, dim3(grid_for((long long)entries * heads)), dim3(256), 0, st, table, entries, heads, packed);
   return cudaGetLastError();
 }
 
