@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) gn_stats_kernel(const void *__restri
                                                             const void *__restrict__ gb, float *mean,
                                                             float *rstd, float *ga, float *gs) {
   constexpr int VW = DT == 0 ? 4 : 8;  // elements per 16-byte vector
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL = 8;
   pdl_trigger();
   pdl_wait();
   cg::cluster_group cl = cg::this_cluster();
@@ -98,16 +98,21 @@ __global__ void __launch_bounds__(kThreads) gn_stats_kernel(const void *__restri
   for (long long i = s0 + tid; i < a0; i += kThreads) chan_merge(st, Stat{1.f, load_scalar<DT>(x, base + i), 0.f});
   const long long nvec = (s1 - a0) / VW;
   const long long a1 = a0 + nvec * VW;
-  // Vector body: UNROLL independent 16-byte loads per step.
+  // Vector body: batches of up to UNROLL independent 16-byte loads per
+  // thread, all issued before any is consumed (one memory round trip per
+  // batch; most slices need a single batch).
   const uint4 *xv = reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(x) +
                                                     (base + a0) * (DT == 0 ? 4 : 2));
-  long long v = tid;
-  for (; v + (long long)(UNROLL - 1) * kThreads < nvec; v += (long long)UNROLL * kThreads) {
+  for (long long v = tid; v < nvec; v += (long long)UNROLL * kThreads) {
     uint4 r[UNROLL];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) r[u] = __ldg(xv + v + (long long)u * kThreads);
+    for (int u = 0; u < UNROLL; ++u) {
+      const long long idx = v + (long long)u * kThreads;
+      r[u] = idx < nvec ? __ldg(xv + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
+      if (v + (long long)u * kThreads >= nvec) break;
       float f[VW];
       if (DT == 0) {
         f[0] = __uint_as_float(r[u].x); f[1] = __uint_as_float(r[u].y);
@@ -122,22 +127,6 @@ __global__ void __launch_bounds__(kThreads) gn_stats_kernel(const void *__restri
       }
       chan_merge(st, chunk_stat<VW>(f));
     }
-  }
-  for (; v < nvec; v += kThreads) {
-    const uint4 r = __ldg(xv + v);
-    float f[VW];
-    if (DT == 0) {
-      f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
-      f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
-    } else {
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        f[2 * k] = __uint_as_float(w[k] << 16);
-        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-      }
-    }
-    chan_merge(st, chunk_stat<VW>(f));
   }
   // Scalar tail.
   for (long long i = a1 + tid; i < s1; i += kThreads) chan_merge(st, Stat{1.f, load_scalar<DT>(x, base + i), 0.f});
@@ -212,7 +201,10 @@ cudaError_t launch_gn_stats(const void *x, int B, int C, int N, int G, int dtype
   const int groups = B * G;
   const long long bytes = (long long)(C / G) * N * (dtype == 0 ? 4 : 2);
   int cs = 1;
-  while (cs < 8 && (long long)groups * cs < 2LL * num_sms && bytes / (2LL * cs) >= 16384) cs *= 2;
+  // Split a group over a cluster of up to 8 CTAs while the doubled grid still
+  // fits one wave (clusters of 8 of these CTAs fit ~51 at a time, so a
+  // larger grid leaves a partial second wave for this latency-bound pass).
+  while (cs < 8 && (long long)groups * cs * 2 <= 2LL * num_sms && bytes / (2LL * cs) >= 16384) cs *= 2;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cs, groups, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
