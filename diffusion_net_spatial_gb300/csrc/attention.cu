@@ -43,7 +43,8 @@ namespace {
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int BLK = 16384;  // one [128 x 64] fp16 swizzled block
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;   // double mode: producer, MMA, four softmax warps
+constexpr int STHREADS = 320;  // single mode with variants: producer, MMA, eight softmax warps
 constexpr int MAX_SMEM_FALLBACK = 232448;
 constexpr int SM_SMEM_PER_TWO = 115712;  // per-CTA budget when two CTAs share an SM
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -66,8 +67,10 @@ struct AttnArgs {
   uint64_t timeout_ns;
 };
 
+// full[nst], empty[nst], q_full, s_full[2], s_free, p_full, o_done, drain, xbar[4]
+__host__ __device__ inline int nbars(int nst) { return 2 * nst + 11; }
 struct Layout {
-  uint32_t q, p, ring, bars;
+  uint32_t q, p, ring, bars, xch;
 };
 __host__ __device__ inline Layout layout(int nqb, int nst, int slot, int p_tmem) {
   Layout L;
@@ -75,12 +78,11 @@ __host__ __device__ inline Layout layout(int nqb, int nst, int slot, int p_tmem)
   L.p = nqb * 16384;
   L.ring = L.p + (p_tmem ? 0 : 32768);
   L.bars = L.ring + nst * slot;
+  L.xch = L.bars + nbars(nst) * 8 + 16;  // [2][2][128] f32 (single mode)
   return L;
 }
-// full[nst], empty[nst], q_full, s_full[2], s_free, p_full, o_done, drain
-__host__ __device__ inline int nbars(int nst) { return 2 * nst + 7; }
 __host__ __device__ inline uint32_t smem_bytes(int nqb, int nst, int slot, int p_tmem) {
-  return layout(nqb, nst, slot, p_tmem).bars + nbars(nst) * 8 + 16 + 1024;
+  return layout(nqb, nst, slot, p_tmem).xch + 2048 + 1024;
 }
 
 // Attention variants on one thread's scores (HNDL attention operator page,
@@ -189,7 +191,7 @@ __device__ __forceinline__ bool apply_variants(uint32_t (&r)[NC][32], const Attn
 // table reads).  Separate instantiations keep the plain block's register
 // budget.
 template <bool SINGLE, int VAR>
-__global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
+__global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SINGLE ? 2 : 1)
     attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -207,6 +209,8 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
   uint64_t *p_full = s_free + 1;
   uint64_t *o_done = p_full + 1;
   uint64_t *drain = o_done + 1;
+  uint64_t *xbar = drain + 1;  // [4] HALVES: row-maximum exchange of the two halves of a row
+  constexpr bool HALVES = SINGLE && VAR != 0;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nbars(nst));
   volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -233,8 +237,9 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     mbar_init(q_full, 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
+    mbar_init(s_free, HALVES ? 8 : 4);
+    mbar_init(p_full, HALVES ? 8 : 4);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -413,26 +418,37 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // HALVES (single mode with a mask or a table): eight warps, warp (q4,
+    // half) takes rows q4*32 .. +31 and keys half*64 .. +63 of each tile; the
+    // two halves of a row exchange their maxima through shared memory and
+    // add their row sums at the end -- twice the independent softmax work per
+    // SM for the heavier per-score work of the variants.  Otherwise four
+    // warps with whole rows (for the plain block the per-tile exchange cost
+    // more than the extra warps gave: unet-l1 119 vs 111 us).
+    constexpr int NC = HALVES ? 2 : 4;  // 32-key chunks per thread per tile
     const int q4 = warp & 3;
+    const int half = HALVES ? ((warp - 2) >> 2) : 0;
     const int row = q4 * 32 + lane;
     const int query = q0 + row;
+    const int kofs = half * (NC * 32);  // first key of this warp within a tile
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     const uint32_t p_tile = smem_u32(sm + L.p);
+    float *xch = reinterpret_cast<float *>(sm + L.xch);  // [2 parity][2 half][128] (HALVES)
     const float sl2 = args.sl2;
     // With a mask or a bias the scores are first turned into base-2 logits
     // (apply_variants), so the scale below becomes 1.
     constexpr bool var = VAR != 0;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    if (VAR == 1) rel_prefetch<4>(args, bh % args.h, query, 0, lane);
+    if (VAR == 1) rel_prefetch<NC>(args, bh % args.h, query, kofs, lane);
     for (int j = 0; j < n; ++j) {
       const int buf = single ? 0 : (j & 1);
       const uint32_t par = single ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
       if (!mbar_wait_warp(&s_full[buf], par, ab)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[4][32];
+      uint32_t r[NC][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + (uint32_t)(buf * BKV + 32 * c), r[c]);
+      for (int c = 0; c < NC; ++c) tmem_ld32(lane_base + (uint32_t)(buf * BKV + kofs + 32 * c), r[c]);
       tmem_wait_ld();
       if (single) {
         // S has been read into registers: the MMA may overwrite it.
@@ -440,34 +456,44 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);
       }
-      const int kvalid = min(BKV, args.N - j * BKV);
-      if (kvalid < BKV) {
+      const int kvalid = min(BKV, args.N - j * BKV) - kofs;
+      if (kvalid < NC * 32) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
       float sc = sl2;  // base-2 logits when the table was added
-      if (var && apply_variants<4, VAR == 2>(r, args, bh % args.h, query, j * BKV, sl2, lane)) sc = 1.f;
-      if (VAR == 1 && j + 1 < n) rel_prefetch<4>(args, bh % args.h, query, (j + 1) * BKV, lane);
-      // Row maximum: eight independent 3-input max chains.
-      float pm[8];
+      if (var && apply_variants<NC, VAR == 2>(r, args, bh % args.h, query, j * BKV + kofs, sl2, lane)) sc = 1.f;
+      if (VAR == 1 && j + 1 < n) rel_prefetch<NC>(args, bh % args.h, query, (j + 1) * BKV + kofs, lane);
+      // Row maximum: 2*NC independent 3-input max chains.
+      float pm[2 * NC];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int t = 0; t < 2 * NC; ++t) {
         const int c = t >> 1, o = (t & 1) * 16;
         float m = __uint_as_float(r[c][o]);
 #pragma unroll
         for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
         pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
       }
-      const float mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+      float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
+      if (NC == 4) mx = max3f(mx, max3f(pm[NC], pm[NC + 1], pm[NC + 2]), pm[2 * NC - 1]);
+      if (HALVES) {
+        // The other half of this row (same lanes, other warp).
+        xch[((j & 1) * 2 + half) * 128 + row] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[q4]);
+        if (!mbar_wait_warp(&xbar[q4], (uint32_t)(j & 1), ab)) { ok = false; break; }
+        mx = fmaxf(mx, xch[((j & 1) * 2 + (half ^ 1)) * 128 + row]);
+      }
       const float m_new = fmaxf(m_used, mx * sc);
       // Lazy rescale: a row raises its reference maximum only when the new
       // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
       // per warp (any row that needs it), because the tensor-memory accesses
       // that rescale O are warp-collective; rows that did not need it use
-      // their own (possibly unit) factor.
+      // their own (possibly unit) factor.  Both halves of a row see the same
+      // maxima, so they decide alike.
       const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
       const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
       float alpha = 1.f;
@@ -482,9 +508,9 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       const uint64_t c2 = f2_pack(sc, sc);
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
+      uint32_t pk[NC / 2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < NC; ++c)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float t0, t1;
@@ -503,7 +529,7 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       if (rescale) {
         __syncwarp();
         tc_fence_after();
-        for (int cc = 0; cc < args.d_o / 16; ++cc) {
+        for (int cc = half; cc < args.d_o / 16; cc += (HALVES ? 2 : 1)) {
           uint32_t t[16];
           tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
           tmem_wait_ld();
@@ -515,16 +541,18 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       }
       if (p_tmem) {
         // P as fp16 pairs in tensor memory: over the S buffer just read
-        // (double) or in its own 64 columns (single).
-        const uint32_t pcol = single ? (uint32_t)args.p_col : (uint32_t)(buf * BKV);
+        // (double) or in its own 64 columns (single; with halves, this half's 32).
+        const uint32_t pcol = single ? (uint32_t)args.p_col + (uint32_t)(half * 32) : (uint32_t)(buf * BKV);
         __syncwarp();
-        tmem_st32(lane_base + pcol, pk[0]);
-        tmem_st32(lane_base + pcol + 32, pk[1]);
+#pragma unroll
+        for (int c2i = 0; c2i < NC / 2; ++c2i) tmem_st32(lane_base + pcol + (uint32_t)(32 * c2i), pk[c2i]);
         tmem_wait_st();
       } else {
+        // P as a [128 x 128] fp16 tile of two 64-key swizzled blocks; this
+        // warp's keys are block `half` (single) or both blocks (double).
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(p_tile + (c >> 3) * 16384 + sw128_offset((uint32_t)row, (uint32_t)(c & 7)),
+        for (int c = 0; c < 4 * NC; ++c)
+          st_shared_v4(p_tile + (half + (c >> 3)) * 16384 + sw128_offset((uint32_t)row, (uint32_t)(c & 7)),
                        pk[c >> 3][(4 * c) & 31], pk[c >> 3][(4 * c + 1) & 31], pk[c >> 3][(4 * c + 2) & 31],
                        pk[c >> 3][(4 * c + 3) & 31]);
         fence_proxy_async_smem();
@@ -534,14 +562,23 @@ __global__ void __launch_bounds__(THREADS, SINGLE ? 2 : 1)
       if (lane == 0) mbar_arrive(p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait_warp(o_done, (n - 1) & 1, ab)) {
+    bool eok = ok && mbar_wait_warp(o_done, (n - 1) & 1, ab);
+    if (HALVES && eok) {
+      // Row sum of the two halves (exchange slot of parity n).
+      xch[((n & 1) * 2 + half) * 128 + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[q4]);
+      eok = mbar_wait_warp(&xbar[q4], (uint32_t)(n & 1), ab);
+      if (eok) l += xch[((n & 1) * 2 + (half ^ 1)) * 128 + row];
+    }
+    if (eok) {
       __syncwarp();
       tc_fence_after();
       const float inv = 1.0f / l;
       const int b = bh / args.h, hd = bh % args.h;
       const bool vec = (args.d % 8) == 0;
       uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
-      for (int cc = 0; cc < args.d_o / 16; ++cc) {
+      for (int cc = half; cc < args.d_o / 16; cc += (HALVES ? 2 : 1)) {
         uint32_t t[16];
         tmem_ld16(lane_base + TM_O + (uint32_t)(cc * 16), t);
         tmem_wait_ld();
@@ -1511,7 +1548,7 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   if (a.single) {
     auto kern = var == 2 ? attention_kernel<true, 2> : (var == 1 ? attention_kernel<true, 1> : attention_kernel<true, 0>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    (void)launch_k(kern, dim3(grid), dim3(THREADS), smem, st, qmap, kmap, vmap, a);
+    (void)launch_k(kern, dim3(grid), dim3(var ? STHREADS : THREADS), smem, st, qmap, kmap, vmap, a);
   } else {
     auto kern =
         var == 2 ? attention_kernel<false, 2> : (var == 1 ? attention_kernel<false, 1> : attention_kernel<false, 0>);
