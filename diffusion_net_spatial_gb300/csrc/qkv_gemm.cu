@@ -306,20 +306,25 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------------------
 // Resident-tile variant (C <= 512): one CTA owns a 128-pixel tile and a group
-// of BN-feature slices.  The tile's GN-applied, transposed fp16 A operand
-// (128 x C) is built once into shared memory and stays there while the CTA
-// sweeps its slices, so x is read and converted once per tile instead of once
-// per slice, and slice i's epilogue overlaps slice i+1's MMAs (two TMEM
-// accumulators).
+// of BN-feature slices (BN <= 128).  The tile's GN-applied, transposed fp16 A
+// operand (128 pixels x C) is built once into tensor-memory columns
+// 256..511 and stays there while the CTA sweeps its slices (A from tensor
+// memory, N = BN MMAs into two alternating 128-column accumulators), so x is
+// read and converted once per tile, slice i's epilogue overlaps slice i+1's
+// MMAs, and all of shared memory is a deep ring for the weight stream (every
+// CTA reads all 3C x C weights; a 3-slot ring behind a shared-memory A tile
+// fed them at ~40 GB/s per SM).
 //   warps 0, 10  TMA producers on alternate ring loads: first the tile's x
-//                blocks [64 channels][128 pixels], then the weight tiles
-//                [BN][64] of every slice
+//                blocks [64 channels][128 pixels], then the weights, two
+//                [BN][64] k-blocks per 32 KB slot
 //   warp 1       MMA warp (warp-uniform loop, elected lane issues)
-//   warps 2..9   converters (x block -> A block), then epilogues (bias, fp16,
-//                direct stores into Q/K rows and V^T rows)
-constexpr int RNST = 3;                  // ring slots of 32 KB
+//   warps 2..9   converters (x block -> A columns in tensor memory), then
+//                epilogues (bias, fp16, direct stores into Q/K rows and V^T
+//                rows)
+constexpr int RNST = 6;                  // ring slots of 32 KB
 constexpr int RSLOT = 32768;
 constexpr int RTHREADS = 352;
+constexpr uint32_t RA_COL = 256;         // A operand: tensor-memory columns 256 .. 256 + C/2
 
 struct ResArgs {
   int C, N, h, dp, ldq, ldn, BN, nkb, nslices, spg, xbytes;
@@ -334,10 +339,9 @@ struct ResArgs {
 };
 // barriers: full[RNST], empty[RNST], xfree[RNST], a_ready, acc_full[2], acc_empty[2], drain
 constexpr int RNBARS = 3 * RNST + 6;
-__host__ __device__ inline uint32_t res_ring_off(int nkb) { return (uint32_t)nkb * 16384u; }
-__host__ __device__ inline uint32_t res_slot_off(int nkb) { return res_ring_off(nkb) + RNST * RSLOT; }
-__host__ __device__ inline uint32_t res_bars_off(int nkb) { return res_slot_off(nkb) + NCONV * 256; }
-__host__ __device__ inline uint32_t res_smem(int nkb) { return res_bars_off(nkb) + RNBARS * 8 + 16; }
+constexpr uint32_t RES_SLOT_OFF = RNST * RSLOT;              // converters' GN scale/shift staging
+constexpr uint32_t RES_BARS_OFF = RES_SLOT_OFF + NCONV * 256;
+constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
 
 template <int DT>
 __global__ void __launch_bounds__(RTHREADS, 1)
@@ -352,7 +356,8 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     return;
   }
   const int nkb = args.nkb;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + res_bars_off(nkb));
+  const int nwl = (nkb + 1) / 2;  // weight loads per slice (two k-blocks each)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + RES_BARS_OFF);
   uint64_t *full = bars;
   uint64_t *empty = bars + RNST;
   uint64_t *xfree = bars + 2 * RNST;
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   uint64_t *drain = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + RNBARS);
   volatile uint32_t *abort_flag = tmem_slot + 1;
-  uint8_t *ring = sm + res_ring_off(nkb);
+  uint8_t *ring = sm;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x;
@@ -370,7 +375,8 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int b = blockIdx.z;
   const int sl0 = g * args.spg;
   const int nsl = min(args.spg, args.nslices - sl0);  // slices of this CTA
-  const int nloads = nkb + nsl * nkb;                  // x blocks, then weight tiles
+  const int nloads = nkb + nsl * nwl;                  // x blocks, then weight pairs
+  const uint32_t wbytes = (uint32_t)args.BN * BK * 2;  // one [BN][64] k-block
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RNST; ++i) {
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     // ------------------------------------------------------------ producers
     // Load t uses slot t mod RNST.  Before refilling a slot the producer waits
     // for the release of the slot's previous load: by the converters (xfree)
-    // for an x block, by the MMA's commit (empty) for a weight tile.  Each
+    // for an x block, by the MMA's commit (empty) for a weight pair.  Each
     // barrier completes once per load of its kind in that slot, in order.
     if (lane == 0) {
       const int me = warp == 0 ? 0 : 1;
@@ -427,9 +433,11 @@ __global__ void __launch_bounds__(RTHREADS, 1)
           mbar_arrive_expect_tx(&full[s], (uint32_t)args.xbytes);
           tma_load_3d(ring + s * RSLOT, &xmap, &full[s], p0, t * BK, b);
         } else {
-          const int i = (t - nkb) / nkb, kb = (t - nkb) % nkb;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(args.BN * BK * 2));
-          tma_load_2d(ring + s * RSLOT, &wmap, &full[s], kb * BK, (sl0 + i) * args.BN);
+          const int i = (t - nkb) / nwl, kp = (t - nkb) % nwl;
+          const int kb0 = 2 * kp, nk = min(2, nkb - kb0);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nk * wbytes);
+          for (int u = 0; u < nk; ++u)
+            tma_load_2d(ring + s * RSLOT + u * wbytes, &wmap, &full[s], (kb0 + u) * BK, (sl0 + i) * args.BN);
         }
         last = t;
       }
@@ -441,24 +449,29 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA warp
     const uint32_t idesc = idesc_f16(BM, (uint32_t)args.BN);
-    const uint64_t ad = sdesc_k128(smem_u32(sm));
     const uint64_t rd = sdesc_k128(smem_u32(ring));
     bool ok = mbar_wait_warp(a_ready, 0, ab), issued = false;
+    tc_fence_after();
     int t = nkb;
     for (int i = 0; i < nsl && ok; ++i) {
       const int buf = i & 1;
       if (i >= 2 && !mbar_wait_warp(&acc_empty[buf], (uint32_t)(((i >> 1) - 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d = tmem + (uint32_t)(buf * 256);
-      for (int kb = 0; kb < nkb && ok; ++kb, ++t) {
+      const uint32_t d = tmem + (uint32_t)(buf * 128);
+      for (int kp = 0; kp < nwl && ok; ++kp, ++t) {
         const int s = t % RNST;
         if (!mbar_wait_warp(&full[s], (uint32_t)((t / RNST) & 1), ab)) { ok = false; break; }
         tc_fence_after();
+        const int nk = min(2, nkb - 2 * kp);
         if (elect_one()) {
+          for (int u = 0; u < nk; ++u) {
+            const int kb = 2 * kp + u;
+            const uint64_t b0 = rd + (uint64_t)((s * RSLOT + u * (int)wbytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_ss(d, ad + (uint64_t)(kb * 1024 + kk * 2), rd + (uint64_t)(s * (RSLOT >> 4) + kk * 2), idesc,
-                       (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk)  // A: 16 channels = 8 columns per step
+              mma_f16_ts(d, tmem + RA_COL + (uint32_t)(kb * 32 + kk * 8), b0 + (uint64_t)(kk * 2), idesc,
+                         (kb | kk) != 0 ? 1u : 0u);
+          }
           mma_commit(&empty[s]);
         }
         __syncwarp();
@@ -477,11 +490,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ converters
+    // Warp (q4, hc) converts pixels q4*32 + lane (its tensor-memory lanes) and
+    // channels hc*32 .. +31 of each k-block into 16 A columns (fp16 pairs).
     const int cw = warp - 2;                 // 0..7
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int px = q4 * 32 + lane;           // pixel row of the A tile
     const int hc = cw >> 2;                  // channel half of a k-block
-    float *slot = reinterpret_cast<float *>(sm + res_slot_off(nkb) + cw * 256);
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    float *slot = reinterpret_cast<float *>(sm + RES_SLOT_OFF + cw * 256);
     const float *ga = args.ga + (long long)b * args.C;
     const float *gs = args.gs + (long long)b * args.C;
     bool ok = true;
@@ -496,30 +512,28 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       slot[32 + lane] = s_c;
       __syncwarp();
       const uint8_t *xs = ring + s * RSLOT;
-      const uint32_t a_tile = smem_u32(sm + kb * 16384);
+      uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch0 = hc * 32 + j * 8;
-        float z[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float xv;
-          if (DT == 0) {
-            xv = reinterpret_cast<const float *>(xs)[(ch0 + i) * BM + px];
-          } else {
-            const unsigned short u = reinterpret_cast<const unsigned short *>(xs)[(ch0 + i) * BM + px];
-            xv = __uint_as_float(((uint32_t)u) << 16);
-          }
-          z[i] = fmaf(slot[j * 8 + i], xv, slot[32 + j * 8 + i]);
+      for (int i = 0; i < 16; ++i) {
+        const int ch = hc * 32 + 2 * i;
+        float x0, x1;
+        if (DT == 0) {
+          x0 = reinterpret_cast<const float *>(xs)[ch * BM + px];
+          x1 = reinterpret_cast<const float *>(xs)[(ch + 1) * BM + px];
+        } else {
+          x0 = __uint_as_float(((uint32_t)reinterpret_cast<const unsigned short *>(xs)[ch * BM + px]) << 16);
+          x1 = __uint_as_float(((uint32_t)reinterpret_cast<const unsigned short *>(xs)[(ch + 1) * BM + px]) << 16);
         }
-        st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_half2(z[0], z[1]),
-                     pack_half2(z[2], z[3]), pack_half2(z[4], z[5]), pack_half2(z[6], z[7]));
+        // channels past C are zero (their scale and shift are zero)
+        w[i] = pack_half2(fmaf(slot[2 * i], x0, slot[32 + 2 * i]), fmaf(slot[2 * i + 1], x1, slot[32 + 2 * i + 1]));
       }
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&xfree[s]);
+      if (lane == 0) mbar_arrive(&xfree[s]);  // the x block has been read
+      tmem_st16(lane_base + RA_COL + (uint32_t)(kb * 32 + hc * 16), w);
     }
     if (ok) {
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(a_ready);
     }
@@ -544,7 +558,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
           const int f0 = fs + cbase + c32;
           const float bl = __ldg(args.bias + f0 + lane);
           uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(buf * 256 + cbase + c32), r);
+          tmem_ld32(lane_base + (uint32_t)(buf * 128 + cbase + c32), r);
           tmem_wait_ld();
           float v[32];
 #pragma unroll
@@ -589,7 +603,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       } else {
         for (int c16 = hc; c16 < args.BN / 16; c16 += 2) {
           uint32_t r[16];
-          tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(buf * 256 + c16 * 16), r);
+          tmem_ld16(lane_base + (uint32_t)(buf * 128 + c16 * 16), r);
           tmem_wait_ld();
           const int f0 = fs + c16 * 16;
           const int sec = f0 / hdp;
@@ -684,29 +698,46 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
   int max_smem = 232448, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (BN <= 256 && BN * BK * 2 <= RSLOT && BM * BK * es <= RSLOT && (int)res_smem(nkb) <= max_smem) {
+  // Resident tile: A (C/2 columns) must fit tensor-memory columns 256..511,
+  // a slice (BN <= 128 features) one 128-column accumulator.
+  int BNr = 0;
+  for (int bn = 128; bn >= 16; bn -= 16)
+    if (dm.ntot % bn == 0) {
+      BNr = bn;
+      break;
+    }
+  if (nkb <= 8 && BNr > 0 && BM * BK * es <= RSLOT && (int)RES_SMEM <= max_smem) {
+    CUtensorMap wmap_r;
+    {
+      const uint64_t dims[2] = {(uint64_t)dm.C, (uint64_t)dm.ntot};
+      const uint64_t strides[1] = {(uint64_t)dm.ldc * 2};
+      const uint32_t box[2] = {BK, (uint32_t)BNr};
+      if (encode_tiled(&wmap_r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w_qkv, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return 1;
+    }
     int nsm = 148;
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const int mtiles = dm.B * ((dm.N + BM - 1) / BM);
-    const int nslices = dm.ntot / BN;
+    const int nslices = dm.ntot / BNr;
     int ng = nsm / mtiles;
     if (ng < 1) ng = 1;
     if (ng > nslices) ng = nslices;
     const int spg = (nslices + ng - 1) / ng;
     ng = (nslices + spg - 1) / spg;
     ResArgs r{};
-    r.C = dm.C; r.N = dm.N; r.h = dm.h; r.dp = dm.dp; r.ldq = dm.ldq; r.ldn = dm.ldn; r.BN = BN;
+    r.C = dm.C; r.N = dm.N; r.h = dm.h; r.dp = dm.dp; r.ldq = dm.ldq; r.ldn = dm.ldn; r.BN = BNr;
     r.nkb = nkb; r.nslices = nslices; r.spg = spg; r.xbytes = BM * BK * es;
     r.ga = ga; r.gs = gs; r.bias = b_qkv; r.q = q; r.k = k; r.vt = vt;
     r.err = kp.err; r.timeout_ns = kp.timeout_ns;
-    const uint32_t smem = res_smem(nkb);
+    const uint32_t smem = RES_SMEM;
     const dim3 grid(ng, (dm.N + BM - 1) / BM, dm.B);
     if (dtype == 0) {
       cudaFuncSetAttribute(qkv_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap, r);
+      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
     } else {
       cudaFuncSetAttribute(qkv_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap, r);
+      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
