@@ -328,6 +328,7 @@ constexpr uint32_t RA_COL = 256;         // A operand: tensor-memory columns 256
 
 struct ResArgs {
   int C, N, h, dp, ldq, ldn, BN, nkb, nslices, spg, xbytes;
+  int w3d;  // weights as one 3-D box of two 64-channel chunks per slot (C % 64 == 0), else two 2-D boxes
   const float *ga;
   const float *gs;
   const float *bias;
@@ -376,6 +377,11 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int sl0 = g * args.spg;
   const int nsl = min(args.spg, args.nslices - sl0);  // slices of this CTA
   const int nloads = nkb + nsl * nwl;                  // x blocks, then weight pairs
+  // Slices are swept starting at a tile-dependent one: all CTAs walking the
+  // weights in the same order request the same tiles at the same time, and
+  // those L2 lines then serve one request after another (measured ~48 GB/s
+  // per SM of weight feed that way).
+  const int rot = nsl > 0 ? (int)(blockIdx.y % (unsigned)nsl) : 0;
   const uint32_t wbytes = (uint32_t)args.BN * BK * 2;  // one [BN][64] k-block
 
   if (threadIdx.x == 0) {
@@ -435,9 +441,17 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         } else {
           const int i = (t - nkb) / nwl, kp = (t - nkb) % nwl;
           const int kb0 = 2 * kp, nk = min(2, nkb - kb0);
-          mbar_arrive_expect_tx(&full[s], (uint32_t)nk * wbytes);
-          for (int u = 0; u < nk; ++u)
-            tma_load_2d(ring + s * RSLOT + u * wbytes, &wmap, &full[s], (kb0 + u) * BK, (sl0 + i) * args.BN);
+          const int sl = sl0 + (i + rot) % nsl;
+          if (args.w3d) {
+            // One box of two 64-channel chunks x BN rows (a chunk index past
+            // the last reads as zeros).
+            mbar_arrive_expect_tx(&full[s], 2u * wbytes);
+            tma_load_3d(ring + s * RSLOT, &wmap, &full[s], 0, sl * args.BN, kb0);
+          } else {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)nk * wbytes);
+            for (int u = 0; u < nk; ++u)
+              tma_load_2d(ring + s * RSLOT + u * wbytes, &wmap, &full[s], (kb0 + u) * BK, sl * args.BN);
+          }
         }
         last = t;
       }
@@ -544,7 +558,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       const int buf = i & 1;
       if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
-      const int fs = (sl0 + i) * args.BN;
+      const int fs = (sl0 + (i + rot) % nsl) * args.BN;
       const int ncol = args.BN / 2;
       if (args.dp % 32 == 0 && ncol % 32 == 0) {
         // Warp (q4, hc) takes columns [hc * BN/2, (hc+1) * BN/2) of the slice,
@@ -554,18 +568,30 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         // the four 16-byte pieces of one row per store instruction.
         const int cbase = hc * ncol;
         const int j4 = lane & 3, g4 = lane & ~3;
+        // Section, head and offset of the first chunk; later chunks advance
+        // by 32 features (a chunk never straddles a head when dp % 32 == 0).
+        int sec = (fs + cbase) / hdp;
+        int hd = ((fs + cbase) / args.dp) % args.h;
+        int e0 = (fs + cbase) % args.dp;
         for (int c32 = 0; c32 < ncol; c32 += 32) {
           const int f0 = fs + cbase + c32;
-          const float bl = __ldg(args.bias + f0 + lane);
           uint32_t r[32];
           tmem_ld32(lane_base + (uint32_t)(buf * 128 + cbase + c32), r);
+          // The chunk's 32 biases, the same for every lane (broadcast loads).
+          const float4 *bq = reinterpret_cast<const float4 *>(args.bias + f0);
+          float bv[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 t4 = __ldg(bq + k);
+            bv[4 * k] = t4.x;
+            bv[4 * k + 1] = t4.y;
+            bv[4 * k + 2] = t4.z;
+            bv[4 * k + 3] = t4.w;
+          }
           tmem_wait_ld();
           float v[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) + __shfl_sync(0xFFFFFFFFu, bl, k);
-          const int sec = f0 / hdp;
-          const int hd = (f0 / args.dp) % args.h;
-          const int e0 = f0 % args.dp;
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) + bv[k];
           const long long bh = (long long)b * args.h + hd;
           if (sec < 2) {
             uint32_t a[4][4];  // a[k] = this row's 16-byte piece k (features 8k .. 8k+7)
@@ -598,6 +624,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
             __half *dst = reinterpret_cast<__half *>(args.vt) + (bh * args.dp + e0) * args.ldn + pix;
 #pragma unroll
             for (int k = 0; k < 32; ++k) dst[(long long)k * args.ldn] = __float2half_rn(v[k]);
+          }
+          e0 += 32;
+          if (e0 == args.dp) {
+            e0 = 0;
+            if (++hd == args.h) {
+              hd = 0;
+              ++sec;
+            }
           }
         }
       } else {
@@ -708,7 +742,19 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     }
   if (nkb <= 8 && BNr > 0 && BM * BK * es <= RSLOT && (int)RES_SMEM <= max_smem) {
     CUtensorMap wmap_r;
-    {
+    const int w3d = (dm.C % BK == 0) ? 1 : 0;
+    if (w3d) {
+      // W viewed as [64-channel chunk][feature][64 channels]: one box = two
+      // chunks x BN features (32 KB for BN = 128), one TMA per ring slot --
+      // half the TMA instructions of two 2-D boxes.  Only when every chunk
+      // lies inside a row (C % 64 == 0).
+      const uint64_t dims[3] = {64, (uint64_t)dm.ntot, (uint64_t)(dm.C / BK)};
+      const uint64_t strides[2] = {(uint64_t)dm.ldc * 2, 128};
+      const uint32_t box[3] = {BK, (uint32_t)BNr, 2};
+      if (encode_tiled(&wmap_r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, w_qkv, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return 1;
+    } else {
       const uint64_t dims[2] = {(uint64_t)dm.C, (uint64_t)dm.ntot};
       const uint64_t strides[1] = {(uint64_t)dm.ldc * 2};
       const uint32_t box[2] = {BK, (uint32_t)BNr};
@@ -727,7 +773,7 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     ng = (nslices + spg - 1) / spg;
     ResArgs r{};
     r.C = dm.C; r.N = dm.N; r.h = dm.h; r.dp = dm.dp; r.ldq = dm.ldq; r.ldn = dm.ldn; r.BN = BNr;
-    r.nkb = nkb; r.nslices = nslices; r.spg = spg; r.xbytes = BM * BK * es;
+    r.nkb = nkb; r.nslices = nslices; r.spg = spg; r.xbytes = BM * BK * es; r.w3d = w3d;
     r.ga = ga; r.gs = gs; r.bias = b_qkv; r.q = q; r.k = k; r.vt = vt;
     r.err = kp.err; r.timeout_ns = kp.timeout_ns;
     const uint32_t smem = RES_SMEM;
