@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
   const int p0 = blockIdx.x * BM;
   const int b = blockIdx.y;
   const int nloads = nkb * nch;
+  // k-blocks are taken from a tile-dependent one on: CTAs walking the weights
+  // in one order request the same L2 lines at the same time.
+  const int rot = (int)(blockIdx.x % (unsigned)nkb);
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
         const int s = t % ORNST;
         if (t >= ORNST && !mbar_wait(&empty[s], (uint32_t)(((t / ORNST) - 1) & 1), ab)) { ok = false; break; }
         mbar_arrive_expect_tx(&full[s], (uint32_t)(BNc * BK * 2));
-        tma_load_2d(ring + s * ORSLOT, &wmap, &full[s], (t / nch) * BK, (t % nch) * BNc);
+        tma_load_2d(ring + s * ORSLOT, &wmap, &full[s], ((t / nch + rot) % nkb) * BK, (t % nch) * BNc);
         last = t;
       }
       if (*abort_flag) {
@@ -399,14 +402,14 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
     const uint64_t rd = sdesc_k128(smem_u32(ring));
     bool ok = mbar_wait_warp(a_full, 0, ab), issued = false;
     for (int t = 0; t < nloads && ok; ++t) {
-      const int s = t % ORNST, kb = t / nch, c = t % nch;
+      const int s = t % ORNST, kpos = t / nch, kb = (kpos + rot) % nkb, c = t % nch;
       if (!mbar_wait_warp(&full[s], (uint32_t)((t / ORNST) & 1), ab)) { ok = false; break; }
       tc_fence_after();
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_f16_ss(tmem + (uint32_t)(c * BNc), ad + (uint64_t)(kb * 1024 + kk * 2),
-                     rd + (uint64_t)(s * (ORSLOT >> 4) + kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+                     rd + (uint64_t)(s * (ORSLOT >> 4) + kk * 2), idesc, (kpos | kk) != 0 ? 1u : 0u);
         mma_commit(&empty[s]);
       }
       __syncwarp();
