@@ -52,6 +52,7 @@ constexpr float RESCALE_LOG2 = 8.0f;
 struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
   int p_tmem, p_col;  // P in tensor memory (and its column in single mode) or in shared memory
+  int vpack;          // both 64-key halves of a tile's V^T in one ring slot (single mode, d_o <= 64)
   float sl2;  // log2(e) / sqrt(d)
   int causal;          // mask keys after the query token
   const float *rel;    // NULL, or packed relative-position table [h][tabn] (log2 units)
@@ -226,7 +227,9 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
   // Under the causal mask, key tiles past the tile's last query are skipped.
   const int n = args.causal ? min(args.ntiles, (min(q0 + BQ, args.N) - 1) / BKV + 1) : args.ntiles;
   constexpr bool single = SINGLE;
-  const int nvb = 2 * args.nvr;                         // V slots per key tile
+  // V slots per key tile: one when both 64-key halves share a slot (the two
+  // boxes then land vrows * 128 bytes apart), else one per half and row group.
+  const int nvb = args.vpack ? 1 : 2 * args.nvr;
   const int nks = (args.nqb + args.kpb - 1) / args.kpb;  // K slots per key tile
 
   if (threadIdx.x == 0) {
@@ -289,9 +292,17 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
       auto load_v = [&](int j) {
         for (int vb = 0; vb < nvb && ok; ++vb) {
           if (!acquire()) { ok = false; break; }
-          const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(args.vrows * 128));
-          tma_load_3d(sm + L.ring + s * slot, &vmap, &full[s], j * BKV + 64 * vh, oc * args.d_o + vr * args.vrows, bh);
+          if (args.vpack) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * args.vrows * 128));
+            for (int vh = 0; vh < 2; ++vh)
+              tma_load_3d(sm + L.ring + s * slot + vh * args.vrows * 128, &vmap, &full[s], j * BKV + 64 * vh,
+                          oc * args.d_o, bh);
+          } else {
+            const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(args.vrows * 128));
+            tma_load_3d(sm + L.ring + s * slot, &vmap, &full[s], j * BKV + 64 * vh, oc * args.d_o + vr * args.vrows,
+                        bh);
+          }
           advance();
         }
       };
@@ -362,21 +373,23 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
         for (int vb = 0; vb < nvb && ok; ++vb) {
           if (!mbar_wait_warp(&full[s], ph, ab)) { ok = false; break; }
           tc_fence_after();
-          const int vh = vb / args.nvr, vr = vb - vh * args.nvr;
-          const uint32_t d_o = tmem + TM_O + (uint32_t)(vr * args.vrows);
-          const uint64_t b0 = rd + (uint64_t)(s * slot16);
-          const uint32_t first = (j > 0 || vh > 0) ? 1u : 0u;
           if (elect_one()) {
-            if (p_tmem) {
-              const uint32_t a0 = tmem + pcol + (uint32_t)(vh * 32);
+            for (int hh = 0; hh < (args.vpack ? 2 : 1); ++hh) {
+              const int vh = args.vpack ? hh : vb / args.nvr, vr = args.vpack ? 0 : vb - vh * args.nvr;
+              const uint32_t d_o = tmem + TM_O + (uint32_t)(vr * args.vrows);
+              const uint64_t b0 = rd + (uint64_t)(s * slot16) + (uint64_t)((hh * args.vrows * 128) >> 4);
+              const uint32_t first = (j > 0 || vh > 0) ? 1u : 0u;
+              if (p_tmem) {
+                const uint32_t a0 = tmem + pcol + (uint32_t)(vh * 32);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ts(d_o, a0 + (uint32_t)(kk * 8), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
-            } else {
-              const uint64_t a0 = pd + (uint64_t)(vh * 1024);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16_ts(d_o, a0 + (uint32_t)(kk * 8), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+              } else {
+                const uint64_t a0 = pd + (uint64_t)(vh * 1024);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16_ss(d_o, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), idesc_o, (first | kk) ? 1u : 0u);
+              }
             }
             mma_commit(&empty[s]);
           }
@@ -1513,6 +1526,10 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   a.kpb = a.slot / BLK;
   a.vrows = dm.d_o <= a.slot / 128 ? dm.d_o : a.slot / 128;
   a.nvr = (dm.d_o + a.vrows - 1) / a.vrows;
+  // Single mode with d_o <= 64: a tile's two V halves share one slot, so a key
+  // tile takes two ring slots instead of three and four slots prefetch two
+  // tiles (per-stage timing showed P V waiting for V with three).
+  a.vpack = (a.single && a.nvr == 1 && 2 * a.vrows * 128 <= a.slot && (a.vrows % 8) == 0) ? 1 : 0;
   if (nst < 2) return 2;
   a.nst = nst;
   a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
