@@ -138,8 +138,9 @@ ssa_status ssa_forward_static(const void *x, int B, int C, int H, int W, int num
  *   o            [B][N][ldc]           heads concatenated along channels
  */
 
-/* GroupNorm statistics (Welford within a thread, Chan merges across threads
- * and across the CTAs of a cluster): per (b, g) mean and rstd =
+/* GroupNorm statistics (per thread a running count, mean and M2 fed by the
+ * two-pass statistics of each batch of loads; Chan merges across threads and
+ * across the CTAs of a cluster): per (b, g) mean and rstd =
  * 1/sqrt(var_biased + 1e-5), then the folded per-(b, c) affine
  * gn_scale = rstd * norm_weight[c], gn_shift = norm_bias[c] - mean * gn_scale,
  * so that GN(x)[b, c, :] = gn_scale[b, c] * x[b, c, :] + gn_shift[b, c].
