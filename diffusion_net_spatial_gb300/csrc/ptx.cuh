@@ -115,13 +115,6 @@ __device__ __forceinline__ void cluster_sync() {
 }
 // Store into another CTA's shared memory; the bytes count towards the
 // transaction count of the barrier `rbar` in that CTA.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                   raddr),
-               "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
-               : "memory");
-}
 __device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr), "r"(v),
                "r"(rbar)
