@@ -14,8 +14,12 @@ max time ("weak" scaling).  Prints ONE JSON line on rank 0.
 
 --impl reference times the fp64 CPU oracle (the method as defined, plain
 loops) on this machine's host cores instead, on a bounded query sample of the
-same workload, extrapolated to the whole workload by the algorithmic FLOP
-ratio.
+same workload, extrapolated to the whole workload as fixed cost + N x
+per-query cost (the same sample and rule as the cpu_baseline of our arm).
+
+The line also carries, under "also", the block time, TFLOP/s and per-kernel
+split of the other N >= 4096 workload (unet-l1: B=2, C=320, 64 x 64, 8 heads
+of 40), timed the same way; the named workload stays the headline.
 """
 from __future__ import annotations
 
@@ -182,10 +186,18 @@ def kernel_traffic(kernel_file: str, workload: str):
 
 # ----------------------------------------------------------- CPU baseline ---
 
-def oracle_sample(wl, nq: int, seed: int = 0):
-    """Time the fp64 oracle on nq seeded query pixels of the workload (K and V
-    for every pixel), and extrapolate to the whole workload by the ratio of
-    algorithmic FLOPs.  Returns (seconds_measured, seconds_full_estimate)."""
+# Both CPU legs (the bench line's cpu_baseline and the --impl reference arm)
+# time the oracle the same way: a run on a few query pixels measures the part
+# that does not depend on the sample (GN, Z, K and V for every pixel), a run on
+# ORACLE_SAMPLE query pixels adds the per-query part, and the whole workload is
+# estimated as fixed + N * per-query (a straight line through the two runs).
+ORACLE_FIXED_Q = 16
+ORACLE_SAMPLE = 1024
+
+
+def oracle_run(wl, nq: int, seed: int = 0) -> float:
+    """Seconds of one fp64 oracle call on nq seeded query pixels of the
+    workload (K and V for every pixel)."""
     import oracle
     x, p, _ = wls.make_inputs(wl)
     g = torch.Generator().manual_seed(seed)
@@ -194,68 +206,188 @@ def oracle_sample(wl, nq: int, seed: int = 0):
     pf = {k: v.double().numpy() for k, v in p.items()}
     t0 = time.perf_counter()
     oracle.forward(xf, pf, wl.num_groups, wl.num_heads, qidx=qidx)
-    dt = time.perf_counter() - t0
-    B, C, N = wl.B, wl.C, wl.N
-    f_sample = B * (4.0 * N * C * C + nq * (4.0 * C * C + 4.0 * N * C))
-    return dt, dt * wl.flops / f_sample
+    return time.perf_counter() - t0
 
 
-def sample_size(wl, budget_flops: float = 4e11) -> int:
-    """Query sample for a bounded oracle run (seconds to tens of seconds on the host cores)."""
-    B, C, N = wl.B, wl.C, wl.N
-    per_q = B * (4.0 * C * C + 4.0 * N * C)
-    fixed = B * 4.0 * N * C * C
-    nq = int(max(16, (budget_flops - fixed) / per_q))
-    return min(N, nq)
+def oracle_extrapolate(wl, t_fixed: float, t_sample: float, nq: int) -> float:
+    """Whole-workload seconds from a fixed-cost run (ORACLE_FIXED_Q queries)
+    and a sample run (nq queries): fixed + N * per-query."""
+    nq0 = min(ORACLE_FIXED_Q, wl.N)
+    if nq <= nq0:
+        return t_sample
+    per_q = max(t_sample - t_fixed, 0.0) / (nq - nq0)
+    return t_fixed + per_q * (wl.N - nq0)
 
 
-def cpu_baseline(wl) -> dict:
+def cpu_baseline(wl, repeats: int = 3) -> dict:
     import oracle
-    nq = sample_size(wl)
-    dt, full = oracle_sample(wl, nq)
+    nq = min(wl.N, ORACLE_SAMPLE)
+    t_fixed = oracle_run(wl, min(ORACLE_FIXED_Q, wl.N))
+    ts = [oracle_run(wl, nq) for _ in range(repeats)]
+    full = oracle_extrapolate(wl, t_fixed, statistics.median(ts), nq)
     return {"value": wl.tokens / full, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{nq} seeded query pixels of {wl.name} (K,V for all {wl.N} pixels), {dt:.2f}s measured, "
-                      f"extrapolated to the whole workload by the algorithmic FLOP ratio"}
+            "sample": f"{nq} seeded query pixels of {wl.name} (K,V for all {wl.N} pixels), median of {repeats} "
+                      f"runs {statistics.median(ts):.2f}s, plus a {min(ORACLE_FIXED_Q, wl.N)}-query run "
+                      f"{t_fixed:.2f}s for the fixed part; whole workload = fixed + N x per-query"}
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 oracle on host cores (rank 0 only)."""
+    """The reference arm: the fp64 oracle on host cores (rank 0 only), the same
+    sample and extrapolation as the bench line's cpu_baseline."""
     wl = wls.WORKLOADS[args.workload]
     if rank != 0:
         return
     import oracle
     oracle.build()
-    nq = sample_size(wl, budget_flops=1.2e12 / max(1, args.steps))
-    for _ in range(args.warmup):
-        oracle_sample(wl, 16)
-    est = []
-    meas = 0.0
-    for _ in range(args.steps):
-        dt, full = oracle_sample(wl, nq)
-        meas += dt
-        est.append(full)
-    t_step = statistics.mean(est)
+    nq = min(wl.N, ORACLE_SAMPLE)
+    fixed = [oracle_run(wl, min(ORACLE_FIXED_Q, wl.N)) for _ in range(max(1, args.warmup))]
+    t_fixed = statistics.median(fixed)
+    ts = [oracle_run(wl, nq) for _ in range(args.steps)]
+    t_step = oracle_extrapolate(wl, t_fixed, statistics.mean(ts), nq)
     value = wl.tokens / t_step
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(wl, "oracle, query-sampled"),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "ms_per_step_kind": "extrapolated to the whole workload from query-sampled runs (see cpu_baseline.sample)",
+        "sample_ms_per_step": statistics.mean(ts) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl), "mode": "fp64 CPU oracle, query-sampled and extrapolated",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{nq} seeded query pixels per step (K,V for all pixels), {meas:.1f}s measured, "
-                                   f"extrapolated by the algorithmic FLOP ratio"},
+                         "sample": f"{nq} seeded query pixels per step (K,V for all {wl.N} pixels), mean "
+                                   f"{statistics.mean(ts):.2f}s per step over {args.steps} steps, plus "
+                                   f"{len(fixed)} warm-up runs of {min(ORACLE_FIXED_Q, wl.N)} queries "
+                                   f"({t_fixed:.2f}s) for the fixed part; whole workload = fixed + N x per-query"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, mode: str) -> dict:
+def config_of(wl) -> dict:
+    """The workload, identical for both arms (how each arm runs it is in the
+    line's "mode")."""
     return {"workload": wl.name, "B": wl.B, "C": wl.C, "H": wl.H, "W": wl.W, "num_groups": wl.num_groups,
-            "num_heads": wl.num_heads, "x_dtype": wl.dtype, "mode": mode,
+            "num_heads": wl.num_heads, "x_dtype": wl.dtype,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)", "seed": wl.seed}
 
 
+OUR_MODE = ("planned forward (parameters packed once); tensor-core operands fp16 (not bf16), fp32 accumulation, "
+            "fp32 softmax statistics; result in x's dtype")
+
+
 # ---------------------------------------------------------------- our arm ---
+
+def time_block(ssa, plan, xd, out, ws, flush, stream, warmup: int, steps: int):
+    """Warm-up steps, then `steps` timed planned forwards, each bracketed by
+    its own event pair on the launching stream, with the L2 flushed before
+    each (outside the events).  Returns (status, seconds of the timed steps)."""
+    dev = xd.device
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            plan.forward(xd, out=out, workspace=ws, stream=stream)
+    st = ssa.ssa_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+    if steps == 0:
+        return st, 0.0
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            starts[i].record(stream)
+            plan.forward(xd, out=out, workspace=ws, stream=stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    st = ssa.ssa_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+    return st, sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+
+KERNELS = ["gn_stats", "qkv_gemm", "attention", "out_proj"]
+
+
+def kernel_breakdown(ssa, wl, xd, pd, out, flush, stream, kb: int) -> dict:
+    """Mean event-timed duration (ms) of each kernel of the block, launched
+    step by step through the per-step entry points with the planned layouts
+    (the attention step gets the same scratch the planned forward gives it)."""
+    dev = xd.device
+    with torch.cuda.stream(stream):
+        pk = ssa.ssa_pack_weights(pd, wl.num_heads, stream=stream)
+    per = {n: [] for n in KERNELS}
+    ws_att_bytes = ssa.attention_workspace_size(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
+    ws_att = torch.empty(ws_att_bytes, dtype=torch.uint8, device=dev) if ws_att_bytes else None
+    with torch.cuda.stream(stream):
+        for i in range(kb + 2):
+            flush.fill_(i & 0xFF)
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
+            _, _, a, s = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"], stream=stream)
+            ev[1].record(stream)
+            q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], wl.num_heads, stream=stream)
+            ev[2].record(stream)
+            o = ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads, stream=stream, workspace=ws_att)
+            ev[3].record(stream)
+            ssa.ssa_out_project(o, pk["w_o"], pk["b_o"], xd, out=out, stream=stream)
+            ev[4].record(stream)
+            if i >= 2:
+                torch.cuda.synchronize(dev)
+                for j, n in enumerate(KERNELS):
+                    per[n].append(ev[j].elapsed_time(ev[j + 1]))
+    torch.cuda.synchronize(dev)
+    st = ssa.ssa_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+    return {n: statistics.mean(v) for n, v in per.items()}
+
+
+def roofline(wl, kern_ms: dict, peaks: dict) -> dict:
+    """Roofline entry of the dominant kernel: algorithmic FLOPs (bytes for the
+    GN statistics pass) per launch over its mean event-timed duration."""
+    B, C, N = wl.B, wl.C, wl.N
+    flops_k = {"gn_stats": 0.0, "qkv_gemm": 6.0 * B * N * C * C, "attention": 4.0 * B * N * N * C,
+               "out_proj": 2.0 * B * N * C * C}
+    dominant = max(kern_ms, key=kern_ms.get)
+    if dominant == "gn_stats":
+        achieved = B * C * N * (4 if wl.dtype == "f32" else 2) / (kern_ms[dominant] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = flops_k[dominant] / (kern_ms[dominant] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(dominant, wl.name)
+    roof["kernel"] = dominant
+    roof["peak_source"] = (f"{peaks['source']} bf16 dense burst (fp16 operands: same nominal tensor rate)"
+                           if roof["bound"] == "tensor" else f"{peaks['source']} HBM copy")
+    return roof
+
+
+def also_workload(ssa, name: str, steps: int, flush, stream, peaks) -> dict:
+    """Block time, TFLOP/s and per-kernel split of another workload, timed as
+    the headline (planned forward, L2 flushed between steps)."""
+    wl = wls.WORKLOADS[name]
+    dev = flush.device
+    x, p, _ = wls.make_inputs(wl)
+    with torch.cuda.stream(stream):
+        xd = x.to(dev)
+        pd = {k: v.to(dev) for k, v in p.items()}
+        plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads, stream=stream)
+        out = torch.empty_like(xd)
+        ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=dev)
+    time_block(ssa, plan, xd, out, ws, flush, stream, 5, 0)
+    secs = time_block(ssa, plan, xd, out, ws, flush, stream, 0, steps)[1]
+    kern_ms = kernel_breakdown(ssa, wl, xd, pd, out, flush, stream, max(3, min(steps, 20)))
+    tflops = wl.flops * steps / secs / 1e12
+    plan.close()
+    return {"ms_per_step": secs / steps * 1e3, "value": wl.tokens * steps / secs, "unit": UNIT,
+            "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "pct_of_bf16_sustained_peak": tflops / peaks["bf16_tflops_sustained"],
+            "kernels_ms": kern_ms, "roofline": roofline(wl, kern_ms, peaks),
+            "config": config_of(wl), "mode": OUR_MODE}
+
 
 def run_ours(args, rank, world, local):
     import diffusion_net_spatial_gb300 as ssa
@@ -273,87 +405,19 @@ def run_ours(args, rank, world, local):
         ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=dev)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step():
-        plan.forward(xd, out=out, workspace=ws, stream=stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-    st = ssa.ssa_get_device_status(stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
-
-    # ---- timed region: the whole block, one event pair per step
+    st = time_block(ssa, plan, xd, out, ws, flush, stream, max(3, args.warmup), 0)[0]
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            for i in range(K):
-                flush.fill_(i & 0xFF)
-                torch.cuda._sleep(HOST_LEAD_CYCLES)
-                starts[i].record(stream)
-                step()
-                ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+        total_s = time_block(ssa, plan, xd, out, ws, flush, stream, 0, K)[1]
     barrier(world)
-    st = ssa.ssa_get_device_status(stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_s = sum(ms) / 1e3
     agg = aggregate(wl.tokens * K, total_s, world)
     ms_per_step = agg["seconds"] / K * 1e3
     tflops = wl.flops * K * world / agg["seconds"] / 1e12
-
-    # ---- per-kernel breakdown (same kernels, launched step by step)
-    lay = ssa.layout(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
-    with torch.cuda.stream(stream):
-        pk = ssa.ssa_pack_weights(pd, wl.num_heads, stream=stream)
-    names = ["gn_stats", "qkv_gemm", "attention", "out_proj"]
-    per = {n: [] for n in names}
-    # the attention step with the same scratch the planned forward gives it
-    ws_att_bytes = ssa.attention_workspace_size(wl.B, wl.C, wl.H, wl.W, wl.num_heads)
-    ws_att = torch.empty(ws_att_bytes, dtype=torch.uint8, device=dev) if ws_att_bytes else None
     kb = max(3, min(K, 20))
-    with torch.cuda.stream(stream):
-        for i in range(kb + 2):
-            flush.fill_(i & 0xFF)
-            torch.cuda._sleep(HOST_LEAD_CYCLES)
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-            ev[0].record(stream)
-            _, _, a, s = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"], stream=stream)
-            ev[1].record(stream)
-            q, k, vt = ssa.ssa_qkv_project(xd, a, s, pk["w_qkv"], pk["b_qkv"], wl.num_heads, stream=stream)
-            ev[2].record(stream)
-            o = ssa.ssa_attention_ex(q, k, vt, wl.B, wl.C, wl.H, wl.W, wl.num_heads, stream=stream, workspace=ws_att)
-            ev[3].record(stream)
-            ssa.ssa_out_project(o, pk["w_o"], pk["b_o"], xd, out=out, stream=stream)
-            ev[4].record(stream)
-            if i >= 2:
-                per_i = ev
-                torch.cuda.synchronize(dev)
-                for j, n in enumerate(names):
-                    per[n].append(per_i[j].elapsed_time(per_i[j + 1]))
-    torch.cuda.synchronize(dev)
-    kern_ms = {n: statistics.mean(v) for n, v in per.items()}
-    B, C, N = wl.B, wl.C, wl.N
-    flops_k = {"gn_stats": 0.0, "qkv_gemm": 6.0 * B * N * C * C, "attention": 4.0 * B * N * N * C,
-               "out_proj": 2.0 * B * N * C * C}
-    dominant = max(kern_ms, key=kern_ms.get)
-    if dominant == "gn_stats":
-        achieved = B * C * N * (4 if wl.dtype == "f32" else 2) / (kern_ms[dominant] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        achieved = flops_k[dominant] / (kern_ms[dominant] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = kernel_traffic(dominant, wl.name)
-    roof["kernel"] = dominant
-    roof["peak_source"] = (f"{peaks['source']} bf16 dense burst (fp16 operands: same nominal tensor rate)"
-                           if roof["bound"] == "tensor" else f"{peaks['source']} HBM copy")
+    kern_ms = kernel_breakdown(ssa, wl, xd, pd, out, flush, stream, kb)
+    roof = roofline(wl, kern_ms, peaks)
 
     # ---- attention variants (HNDL attention operator page) through the same
     # planned entry point: causal mask, rotary embedding, relative-position
@@ -445,13 +509,18 @@ def run_ours(args, rank, world, local):
     e2e = aggregate(wl.tokens * Ke, e2e_s, world)
     xbytes = x.numel() * x.element_size()
 
+    # ---- the other N >= 4096 workload, timed the same way (not the headline)
+    also = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_also:
+        also["unet-l1"] = also_workload(ssa, "unet-l1", K, flush, stream, peaks)
+
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": config_of(wl, "planned (parameters packed once), fp16 tensor-core operands, fp32 accumulate"),
+        "config": config_of(wl), "mode": OUR_MODE,
         "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
         "pct_of_bf16_sustained_peak": tflops / peaks["bf16_tflops_sustained"],
         "kernels_ms": kern_ms,
@@ -465,6 +534,8 @@ def run_ours(args, rank, world, local):
         "gpu_launches": K * ssa.ssa_launches_per_forward(True),
         "clocks": clk.summary(),
     }
+    if also:
+        line["also"] = also
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
@@ -478,6 +549,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wls.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true", help="skip the second workload's entry")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     try:

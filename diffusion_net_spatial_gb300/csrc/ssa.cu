@@ -722,8 +722,8 @@ extern "C" ssa_status ssa_forward_static(const void *x, int B, int C, int H, int
   ssa_status s = check_shape(B, C, H, W, num_groups, num_heads);
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
-  const void *ptrs[] = {x, norm_weight, norm_bias, q_weight, q_bias, k_weight, k_bias,
-                        v_weight, v_bias, out_weight, out_bias, out};
+  // Biases may be NULL (that projection has no bias), as for ssa_forward.
+  const void *ptrs[] = {x, norm_weight, norm_bias, q_weight, k_weight, v_weight, out_weight, out};
   for (const void *p : ptrs)
     if (!p) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(SSA_ERR_ALIGNMENT, "x and out must be 16-byte aligned");

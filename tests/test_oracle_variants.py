@@ -291,3 +291,65 @@ def test_qk_norm_rows_have_rms_gamma():
     np.testing.assert_allclose(np.linalg.norm(u, axis=-1), 1.0, rtol=1e-13)
     r = oracle.qk_norm(m, 3, np.ones((3, 4))).reshape(5, 3, 4)
     np.testing.assert_allclose(np.sqrt((r ** 2).mean(axis=-1)), 1.0, rtol=1e-13)
+
+
+# ------------------------------------------------ query-sampled mode + variants ---
+# The largest workload is checked on sampled query pixels, so the sampled mode
+# must give the same rows as the full block under every variant: the causal
+# mask and the table index use the query's token position (not its row in the
+# sample), and the rotation turns the sampled Q rows by their own positions.
+
+SAMPLES = [
+    np.array([0, 3, 7, 19]),        # sorted, skipping positions
+    np.array([19, 7, 3, 0]),        # reversed: row t is not position t
+    np.array([13, 2, 18, 6, 11]),   # scattered
+]
+
+
+def _sampled_kwargs(variant, H, W, h, d):
+    qg, kg = _gammas(h, d, seed=H * W)
+    table = _rel_table(H, W, h, seed=5)
+    kw = {
+        "causal": dict(causal=True),
+        "rope": dict(rope=True),
+        "rel": dict(rel_table=table),
+        "qk_norm": dict(q_norm_weight=qg, k_norm_weight=kg),
+        "all": dict(causal=True, rope=True, rel_table=table, q_norm_weight=qg, k_norm_weight=kg),
+    }
+    return kw[variant]
+
+
+@pytest.mark.parametrize("variant", ["causal", "rope", "rel", "qk_norm", "all"])
+@pytest.mark.parametrize("qi", SAMPLES, ids=["sorted", "reversed", "scattered"])
+def test_query_sampled_variants_equal_full_mode(variant, qi):
+    """Sampled rows equal the full block's rows bit for bit, for each variant
+    and all of them together, on a non-square grid (4 x 5)."""
+    B, C, H, W, G, h = 2, 8, 4, 5, 4, 2
+    x, p = _x(B, C, H, W, 61), _params(C, 62)
+    kw = _sampled_kwargs(variant, H, W, h, C // h)
+    full = oracle.forward(x, p, G, h, want=("q", "o"), **kw)
+    part = oracle.forward(x, p, G, h, qidx=qi, want=("q", "o"), **kw)
+    np.testing.assert_array_equal(part["y"], full["y"][:, :, qi])
+    np.testing.assert_array_equal(part["q"], full["q"][:, qi])
+    np.testing.assert_array_equal(part["o"], full["o"][:, qi])
+
+
+@pytest.mark.parametrize("variant", ["causal", "rope", "rel", "rel_causal_rope", "qk_norm_rope_causal"])
+def test_query_sampled_variants_match_torch_composition(variant):
+    """The sampled rows against the torch library routes at the same pixels
+    (reversed sample, so a slip from token position to sample row shows)."""
+    B, C, H, W, G, h = 2, 8, 4, 5, 4, 2
+    x, p = _x(B, C, H, W, 63), _params(C, 64)
+    qi = SAMPLES[1]
+    if variant.startswith("qk_norm"):
+        qg, kg = _gammas(h, C // h, seed=65)
+        y_ref = _torch_qk_route(x, p, G, h, qg, kg, rope=True, causal=True)
+        kw = dict(q_norm_weight=qg, k_norm_weight=kg, rope=True, causal=True)
+    else:
+        table = _rel_table(H, W, h, seed=66) if variant.startswith("rel") else None
+        causal = "causal" in variant
+        rope = "rope" in variant
+        y_ref = _torch_route(x, p, G, h, causal=causal, rope=rope, rel=table)
+        kw = dict(causal=causal, rope=rope, rel_table=table)
+    y = oracle.forward(x, p, G, h, qidx=qi, **kw)["y"]
+    np.testing.assert_allclose(y, y_ref.reshape(B, C, H * W)[:, :, qi], rtol=1e-10, atol=1e-10)
