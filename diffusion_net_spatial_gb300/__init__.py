@@ -26,8 +26,8 @@ PARAM_KEYS = ("norm_weight", "norm_bias", "q_weight", "q_bias", "k_weight", "k_b
               "v_weight", "v_bias", "out_weight", "out_bias")
 EXPORTS = ("ssa_workspace_size", "ssa_forward", "ssa_plan_create", "ssa_plan_workspace_size",
            "ssa_forward_planned", "ssa_plan_destroy", "ssa_gn_stats", "ssa_pack_weights",
-           "ssa_qkv_project", "ssa_attention", "ssa_out_project", "ssa_get_device_status",
-           "ssa_set_wait_timeout_ns", "ssa_debug_timeout_probe", "ssa_last_error_string",
+           "ssa_qkv_project", "ssa_qkv_project_rope", "ssa_attention", "ssa_out_project", "ssa_get_device_status",
+           "ssa_set_wait_timeout_ns", "ssa_debug_timeout_probe", "ssa_debug_set_producer_stall", "ssa_last_error_string",
            "ssa_launches_per_forward", "ssa_workspace_size_ex", "ssa_forward_ex", "ssa_plan_workspace_size_ex",
            "ssa_forward_planned_ex", "ssa_rope", "ssa_qk_norm", "ssa_pack_rel_table", "ssa_attention_ex",
            "ssa_attention_workspace_size", "ssa_attention_ws", "ssa_set_attention_split")
@@ -69,11 +69,13 @@ def load_library():
         "ssa_gn_stats": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
         "ssa_pack_weights": ([i32, i32, i32] + [vp] * 8 + [vp] * 4 + [vp], i32),
         "ssa_qkv_project": ([vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
+        "ssa_qkv_project_rope": ([vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
         "ssa_attention": ([vp, vp, vp, i32, i32, i32, i32, vp, vp], i32),
         "ssa_out_project": ([vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp], i32),
         "ssa_get_device_status": ([vp], i32),
         "ssa_set_wait_timeout_ns": ([u64], None),
         "ssa_debug_timeout_probe": ([u64, vp], i32),
+        "ssa_debug_set_producer_stall": ([ctypes.c_uint32, ctypes.c_uint32], None),
         "ssa_last_error_string": ([], ctypes.c_char_p),
         "ssa_launches_per_forward": ([i32], i32),
         "ssa_workspace_size_ex": ([i32] * 7 + [vp], sz),
@@ -311,6 +313,23 @@ def ssa_qkv_project(x: torch.Tensor, gn_scale, gn_shift, w_qkv, b_qkv, num_heads
     return q, k, vt
 
 
+def ssa_qkv_project_rope(x: torch.Tensor, gn_scale, gn_shift, w_qkv, b_qkv, num_heads: int, stream=None):
+    """ssa_qkv_project with the rotary embedding applied in the projection's
+    epilogue; returns fp16 (q, k, vt) as ssa_qkv_project."""
+    lib = load_library()
+    _dev_tensor(x, "x")
+    dt = _dtype_code(x)
+    B, C, H, W = x.shape
+    lay = layout(B, C, H, W, num_heads)
+    dev = x.device
+    q = torch.empty(B, num_heads, lay["N"], lay["ldq"], dtype=torch.float16, device=dev)
+    k = torch.empty_like(q)
+    vt = torch.empty(B, num_heads, lay["dp"], lay["ldn"], dtype=torch.float16, device=dev)
+    _check(lib.ssa_qkv_project_rope(_ptr(x), B, C, H, W, num_heads, dt, _ptr(gn_scale), _ptr(gn_shift), _ptr(w_qkv),
+                                    _ptr(b_qkv), _ptr(q), _ptr(k), _ptr(vt), _stream(stream)))
+    return q, k, vt
+
+
 def ssa_attention(q, k, vt, B: int, C: int, N: int, num_heads: int, o=None, stream=None):
     """Returns o fp16 [B, N, ldc] (heads side by side along channels)."""
     lib = load_library()
@@ -398,6 +417,15 @@ def ssa_get_device_status(stream=None) -> int:
 
 def ssa_set_wait_timeout_ns(ns: int):
     load_library().ssa_set_wait_timeout_ns(int(ns))
+
+
+STALL_QKV, STALL_ATTENTION, STALL_OUT_PROJ = 1, 2, 4
+
+
+def ssa_debug_set_producer_stall(kernel_mask: int, after_loads: int):
+    """Test hook: the named kernels' TMA producers stop after `after_loads`
+    loads (0 = off), so their consumers' bounded waits expire."""
+    load_library().ssa_debug_set_producer_stall(int(kernel_mask), int(after_loads))
 
 
 def ssa_debug_timeout_probe(timeout_ns: int, stream=None):

@@ -53,6 +53,7 @@ struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
   int p_tmem, p_col;  // P in tensor memory (and its column in single mode) or in shared memory
   int vpack;          // both 64-key halves of a tile's V^T in one ring slot (single mode, d_o <= 64)
+  int ones;           // single mode, d < dp: V^T row d is all ones, so O column d accumulates the row sums
   float sl2;  // log2(e) / sqrt(d)
   int causal;          // mask keys after the query token
   const float *rel;    // NULL, or packed relative-position table [h][tabn] (log2 units)
@@ -66,6 +67,7 @@ struct AttnArgs {
   uint16_t *o;
   uint32_t *err;
   uint64_t timeout_ns;
+  uint32_t stall;      // test hook (single/double modes): the producer stops after this many ring loads
 };
 
 // full[nst], empty[nst], q_full, s_full[2], s_free, p_full, o_done, drain, xbar[4]
@@ -274,7 +276,10 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
       bool ok = true;
       mbar_arrive_expect_tx(q_full, (uint32_t)(args.nqb * 16384));
       for (int qb = 0; qb < args.nqb; ++qb) tma_load_3d(sm + L.q + qb * 16384, &qmap, q_full, qb * 64, q0, bh);
-      auto acquire = [&]() -> bool { return it < nst || mbar_wait(&empty[s], ph ^ 1u, ab); };
+      auto acquire = [&]() -> bool {
+        if (args.stall && (uint32_t)it >= args.stall) return false;  // test hook: consumers' waits expire
+        return it < nst || mbar_wait(&empty[s], ph ^ 1u, ab);
+      };
       auto advance = [&]() {
         ++it;
         if (++s == nst) { s = 0; ph ^= 1u; }
@@ -313,9 +318,9 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
         if (j + 2 < n) load_k(j + 2);
       }
       // Never leave with a copy in flight.
-      mbar_wait_drain(q_full, 0, ab.limit_ns);
+      mbar_wait_drain(q_full, 0, drain_limit(ab));
       for (int i = (it > nst ? it - nst : 0); i < it; ++i)
-        mbar_wait_drain(&full[i % nst], (i / nst) & 1, ab.limit_ns);
+        mbar_wait_drain(&full[i % nst], (i / nst) & 1, drain_limit(ab));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -422,10 +427,10 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
         issue_pv(j);
         if (!single && j + 2 < n) issue_s(j & 1);
       }
-      if (!ok && issued) {
+      if (issued) {  // every issued MMA completes before tensor memory is freed
         if (elect_one()) mma_commit(drain);
         __syncwarp();
-        mbar_wait_drain(drain, 0, ab.limit_ns);
+        mbar_wait_drain(drain, 0, drain_limit(ab));
       }
     }
     __syncwarp();
@@ -516,28 +521,43 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
         alpha = ex2_approx(m_used - m_new);
         m_used = m_new;
       }
-      // p = 2^(s * log2(e)/sqrt(d) - m): one paired FMA per two scores, the
-      // row sum in four paired accumulators.
+      // p = 2^(s * log2(e)/sqrt(d) - m): one paired FMA per two scores.
       const uint64_t c2 = f2_pack(sc, sc);
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[NC / 2][32];
+      if (args.ones) {
+        // The row sums come from V's column of ones (the P V MMA adds up
+        // exactly the fp16 P it multiplies), so here only P is formed: the
+        // pair of exponents rounded to fp16 once and exponentiated together
+        // (one MUFU operation for two scores, already packed for the MMA).
 #pragma unroll
-      for (int c = 0; c < NC; ++c)
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-          const float e0 = ex2_approx(t0);
-          const float e1 = ex2_approx(t1);
-          acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
-          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_half2(e0, e1);
-        }
-      float s0, s1, s2, s3;
-      f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
-      f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
-      const float sum = (s0 + s1) + (s2 + s3);
-      l = l * alpha + sum;
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ex2_f16x2(pack_half2(t0, t1));
+          }
+      } else {
+        // the row sum in four paired accumulators
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+            const float e0 = ex2_approx(t0);
+            const float e1 = ex2_approx(t1);
+            acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_half2(e0, e1);
+          }
+        float s0, s1, s2, s3;
+        f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+        f2_unpack(f2_add(acc2[2], acc2[3]), s2, s3);
+        const float sum = (s0 + s1) + (s2 + s3);
+        l = l * alpha + sum;
+      }
       if (j > 0 && !mbar_wait_warp(o_done, (j - 1) & 1, ab)) { ok = false; break; }
       if (rescale) {
         __syncwarp();
@@ -576,7 +596,7 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
     }
     // ------------------------------------------------------------ epilogue
     bool eok = ok && mbar_wait_warp(o_done, (n - 1) & 1, ab);
-    if (HALVES && eok) {
+    if (HALVES && eok && !args.ones) {
       // Row sum of the two halves (exchange slot of parity n).
       xch[((n & 1) * 2 + half) * 128 + row] = l;
       __syncwarp();
@@ -587,6 +607,10 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
     if (eok) {
       __syncwarp();
       tc_fence_after();
+      if (args.ones) {
+        l = __uint_as_float(tmem_ld1(lane_base + TM_O + (uint32_t)args.d));  // O column d = sum of P
+        tmem_wait_ld();
+      }
       const float inv = 1.0f / l;
       const int b = bh / args.h, hd = bh % args.h;
       const bool vec = (args.d % 8) == 0;
@@ -926,7 +950,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
       // After an abort no load may still be landing when the CTA leaves.
       if (*abort_flag)
         for (int t = last; t >= 0 && t > last - 2 * nst; t -= 2)
-          mbar_wait_drain(&bars[PB_FULL + t % nst], (uint32_t)((t / nst) & 1), ab.limit_ns);
+          mbar_wait_drain(&bars[PB_FULL + t % nst], (uint32_t)((t / nst) & 1), drain_limit(ab));
     }
     __syncwarp();
   } else if (rank == 0) {
@@ -973,10 +997,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         }
         ++si;
       }
-      if (!ok && issued) {
+      if (issued) {  // every issued MMA completes before tensor memory is freed
         if (elect_one()) mma_commit(&bars[PB_DRAIN]);
         __syncwarp();
-        mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
+        mbar_wait_drain(&bars[PB_DRAIN], 0, drain_limit(ab));
       }
       __syncwarp();
     } else {
@@ -1207,10 +1231,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
         }
         ++si;
       }
-      if (!ok && issued) {
+      if (issued) {  // every issued MMA completes before tensor memory is freed
         if (elect_one()) mma_commit(&bars[PB_DRAIN]);
         __syncwarp();
-        mbar_wait_drain(&bars[PB_DRAIN], 0, ab.limit_ns);
+        mbar_wait_drain(&bars[PB_DRAIN], 0, drain_limit(ab));
       }
       __syncwarp();
     } else {
@@ -1530,12 +1554,15 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
   // tile takes two ring slots instead of three and four slots prefetch two
   // tiles (per-stage timing showed P V waiting for V with three).
   a.vpack = (a.single && a.nvr == 1 && 2 * a.vrows * 128 <= a.slot && (a.vrows % 8) == 0) ? 1 : 0;
+  // V^T row d holds ones whenever d < dp (the weight pack sets that bias)
+  a.ones = (a.single && dm.dp > dm.d) ? 1 : 0;
   if (nst < 2) return 2;
   a.nst = nst;
   a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
   a.o = o;
   a.err = kp.err;
   a.timeout_ns = kp.timeout_ns;
+  a.stall = stall_for(kp, STALL_ATTENTION);
 
   CUtensorMap qmap, kmap, vmap;
   const uint64_t BH = (uint64_t)dm.B * dm.h;

@@ -37,11 +37,27 @@ inline Dims make_dims(int B, int C, int H, int W, int G, int h) {
   return s;
 }
 
+// Q/K packing.  When this returns true the Q and K rows of each head in the
+// packed weight (and bias) are pair-interleaved: packed row 2i holds feature i
+// and row 2i+1 feature i + d/2 (i < d/2), rows >= d are zero.  The rotary
+// embedding (rotate-half) pairs feature i with feature i + d/2, so every pair
+// then sits in two adjacent accumulator columns and the projection's epilogue
+// can rotate it in registers; the epilogue writes every feature back to its
+// own place, so Q and K in memory keep the plain layout.  True for an even
+// head dim that is a multiple of 16 (so both halves of every 8-pair piece
+// start 16-byte aligned) when the resident projection kernel runs
+// (C <= 512), or, for the other kernel, when the head has no padding.
+bool qk_pair_interleaved(const Dims &dm);
+
 // Arguments every pipelined kernel receives for its bounded waits.
 struct KParams {
   uint32_t *err;        // device error word
   uint64_t timeout_ns;  // limit of one spin wait
+  uint32_t stall_mask;  // test hook: kernels whose TMA producers stop early (STALL_* bits)
+  uint32_t stall_after; // ... after this many loads
 };
+enum : uint32_t { STALL_QKV = 1, STALL_ATTENTION = 2, STALL_OUT_PROJ = 4 };
+inline uint32_t stall_for(const KParams &kp, uint32_t bit) { return (kp.stall_mask & bit) ? kp.stall_after : 0u; }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 // dims/strides innermost first; strides in bytes for dims 1..rank-1.
@@ -89,9 +105,10 @@ cudaError_t launch_pack_weights(const Dims &dm, int dtype, const void *wq, const
 cudaError_t launch_pad_x(const void *x, int B, int C, int N, int ldx, int esize, void *dst, cudaStream_t st);
 
 // Returns 0 on success, 1 when a tensor map could not be encoded, 2 on a launch error.
+// rope: Q and K are rotated in the epilogue (requires qk_pair_interleaved(dm)).
 int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const float *ga, const float *gs,
                     const uint16_t *w_qkv, const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt,
-                    const KParams &kp, cudaStream_t st);
+                    const KParams &kp, cudaStream_t st, int rope = 0);
 
 // causal: keys after the query token are masked; rel: NULL or the packed
 // relative-position table [h][(2H-1)(2W-1)] fp32 (times log2 e) over the

@@ -34,6 +34,7 @@ constexpr int THREADS = (2 + NEPI) * 32;
 
 struct OutArgs {
   int C, N, BN, nk, tmem_cols, tma_epi, es;
+  uint32_t stall;  // test hook: the producer stops after this many operand loads (0: never)
   const float *bias;
   const void *x;
   void *out;
@@ -117,14 +118,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       const uint32_t bytes = (uint32_t)(BM * BK * 2 + BN * BK * 2);
       for (; it < nk; ++it) {
+        if (args.stall && (uint32_t)it >= args.stall) break;  // test hook: consumers' waits expire
         const int s = it % ST;
         if (it >= ST && !mbar_wait(&empty[s], ((it / ST) - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
         tma_load_3d(sm + a_off + s * (BM * BK * 2), &omap, &full[s], it * BK, p0, b);
         tma_load_2d(sm + b_off + s * (BN * BK * 2), &wmap, &full[s], it * BK, n0);
       }
-      for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_wait_drain(&full[i % ST], (i / ST) & 1, ab.limit_ns);
-      if (tma_epi) mbar_wait_drain(x_full, 0, ab.limit_ns);
+      for (int i = (it > ST ? it - ST : 0); i < it; ++i) mbar_wait_drain(&full[i % ST], (i / ST) & 1, drain_limit(ab));
+      if (tma_epi) mbar_wait_drain(x_full, 0, drain_limit(ab));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -153,10 +155,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (elect_one()) mma_commit(acc_full);
         __syncwarp();
       }
-      if (!ok && issued) {
+      if (issued) {  // every issued MMA completes before tensor memory is freed
         if (elect_one()) mma_commit(drain);
         __syncwarp();
-        mbar_wait_drain(drain, 0, ab.limit_ns);
+        mbar_wait_drain(drain, 0, drain_limit(ab));
       }
     }
     __syncwarp();
@@ -270,6 +272,7 @@ constexpr int ORTHREADS = 352;
 
 struct OutResArgs {
   int C, N, nkb, nch, BNc, npieces, es;
+  uint32_t stall;  // test hook: each producer stops at this weight-load index (0: never)
   const float *bias;
   uint32_t *err;
   uint64_t timeout_ns;
@@ -358,18 +361,21 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
         for (int k = 0; k < args.npieces; ++k) tma_prefetch_3d(&xmap, p0, k * 128, b);
       }
       int last = -1;
+      bool stalled = false;
       for (int t = me; t < nloads; t += 2) {
+        if (args.stall && (uint32_t)t >= args.stall) { stalled = true; break; }  // test hook
         const int s = t % ORNST;
         if (t >= ORNST && !mbar_wait(&empty[s], (uint32_t)(((t / ORNST) - 1) & 1), ab)) { ok = false; break; }
         mbar_arrive_expect_tx(&full[s], (uint32_t)(BNc * BK * 2));
         tma_load_2d(ring + s * ORSLOT, &wmap, &full[s], ((t / nch + rot) % nkb) * BK, (t % nch) * BNc);
         last = t;
       }
-      if (*abort_flag) {
+      if (*abort_flag || stalled) {
         for (int t = last; t >= 0 && t > last - 2 * ORNST; t -= 2)
-          mbar_wait_drain(&full[t % ORNST], (uint32_t)((t / ORNST) & 1), ab.limit_ns);
-        if (me == 0) mbar_wait_drain(a_full, 0, ab.limit_ns);
+          mbar_wait_drain(&full[t % ORNST], (uint32_t)((t / ORNST) & 1), drain_limit(ab));
+        if (me == 0) mbar_wait_drain(a_full, 0, drain_limit(ab));
       }
+      int nxl[2] = {0, 0};  // residual pieces loaded into each buffer
       if (me == 0 && ok && !*abort_flag) {
         // Residual pieces, once every MMA (the last readers of the shared
         // memory they reuse) has completed.
@@ -377,6 +383,7 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
           for (int k = 0; k < 2 && k < args.npieces; ++k) {
             mbar_arrive_expect_tx(&xfull[k], piece_bytes);
             tma_load_3d(sm + k * piece_bytes, &xmap, &xfull[k], p0, k * 128, b);
+            ++nxl[k];
           }
           for (int k = 0; k < args.npieces; ++k) {
             const int bf = k & 1;
@@ -387,12 +394,15 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
               tma_store_wait_read();  // the buffer's store has read it
               mbar_arrive_expect_tx(&xfull[bf], piece_bytes);
               tma_load_3d(sm + bf * piece_bytes, &xmap, &xfull[bf], p0, (k + 2) * 128, b);
+              ++nxl[bf];
             }
           }
           tma_store_wait_all();
         }
+        // Each buffer's last load (phase nxl - 1) must have landed.
         if (*abort_flag)
-          for (int k = 0; k < 2 && k < args.npieces; ++k) mbar_wait_drain(&xfull[k], 0, ab.limit_ns);
+          for (int k = 0; k < 2; ++k)
+            if (nxl[k] > 0) mbar_wait_drain(&xfull[k], (uint32_t)((nxl[k] - 1) & 1), drain_limit(ab));
       }
     }
     __syncwarp();
@@ -419,10 +429,10 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
       if (elect_one()) mma_commit(acc_full);
       __syncwarp();
     }
-    if (!ok && issued) {
+    if (issued) {  // every issued MMA completes before tensor memory is freed
       if (elect_one()) mma_commit(drain);
       __syncwarp();
-      mbar_wait_drain(drain, 0, ab.limit_ns);
+      mbar_wait_drain(drain, 0, drain_limit(ab));
     }
     __syncwarp();
   } else {
@@ -546,7 +556,7 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
     }
     OutResArgs r{};
     r.C = dm.C; r.N = dm.N; r.nkb = nkb; r.nch = nch; r.BNc = BNc; r.npieces = (dm.C + 127) / 128; r.es = es;
-    r.bias = b_o; r.err = kp.err; r.timeout_ns = kp.timeout_ns;
+    r.bias = b_o; r.err = kp.err; r.timeout_ns = kp.timeout_ns; r.stall = stall_for(kp, STALL_OUT_PROJ);
     const uint32_t smem = ores_smem(nkb);
     const dim3 grid((dm.N + BM - 1) / BM, dm.B, 1);
     if (dtype == 0) {
@@ -563,6 +573,7 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
   a.tmem_cols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
   a.tma_epi = tma_epi; a.es = es;
   a.bias = b_o; a.x = x; a.out = out; a.err = kp.err; a.timeout_ns = kp.timeout_ns;
+  a.stall = stall_for(kp, STALL_OUT_PROJ);
   const uint32_t smem = smem_total(BN, tma_epi, es);
   const dim3 grid((dm.C + BN - 1) / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {

@@ -88,6 +88,15 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
   return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
+// Bound of a drain wait: the in-flight copies and MMAs a CTA waits for
+// before leaving always complete within microseconds, so the drain keeps a
+// floor of 50 ms whatever the (possibly much shorter) limit of the ordinary
+// waits -- a short limit must never let a CTA leave with a copy or an MMA
+// still writing into its shared or tensor memory.
+__device__ __forceinline__ uint64_t drain_limit(const Abort &ab) {
+  return ab.limit_ns > 50000000ull ? ab.limit_ns : 50000000ull;
+}
+
 // Wait used only while cleaning up after an abort: bounded, never raises.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
@@ -350,6 +359,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 32 lanes x 32 bit, one column per thread.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return r;
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -392,6 +407,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// 2^x for two fp16 values at once (low and high halves of a packed pair):
+// one MUFU operation for two results, the output already packed for the MMA.
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 // Packed fp32 pairs (one 64-bit register): Blackwell's paired FMA/ADD issue

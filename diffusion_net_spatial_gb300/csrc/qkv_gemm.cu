@@ -27,6 +27,69 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+
+// Rotary embedding of one pair (HNDL "attention" operator page, Rotary
+// embeddings paragraph: rotate-half, base 10000): feature i (x) and feature
+// i + d/2 (y) of the token at position t turn by angle = t * theta_i,
+// theta_i = 10000^(-2i/d).  theta_i comes as two fp32 parts (hi + lo, formed
+// in fp64); the product t * hi is carried with its exact rounding residual,
+// the angle is reduced to [-pi, pi] by Cody and Waite's two-constant scheme
+// (2 pi = 6.28125 + a small remainder, so k * 6.28125 is exact for the
+// |k| < 2^12 of t < 2^16), and __sincosf, accurate on that interval, gives
+// cos and sin.  The rotation acts on the fp32 accumulator values (bias added)
+// before their single rounding to fp16.
+constexpr float kTwoPiA = 6.28125f;
+constexpr float kTwoPiB = 1.9353071795864769e-3f;  // 2 pi - 6.28125
+constexpr float kInvTwoPi = 0.15915494309189535f;
+
+__device__ __forceinline__ void rope_pair(float &x, float &y, float t, float2 th) {
+  const float a_hi = t * th.x;
+  const float a_lo = fmaf(t, th.y, fmaf(t, th.x, -a_hi));
+  const float k = rintf(a_hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiA, a_hi);
+  r = fmaf(-k, kTwoPiB, r) + a_lo;
+  float sn, c;
+  __sincosf(r, &sn, &c);
+  const float x2 = fmaf(x, c, -y * sn);
+  y = fmaf(y, c, x * sn);
+  x = x2;
+}
+
+// theta_i = 10000^(-2i/d) for i < d/2, split into fp32 hi + lo, into the
+// shared-memory table th[] (one entry per thread of the caller's range).
+__device__ __forceinline__ void rope_thetas(float2 *th, int d, int tid, int nthreads) {
+  for (int i = tid; i < d / 2; i += nthreads) {
+    const double v = exp(-2.0 * (double)i / (double)d * 9.2103403719761827361);  // ln(10000)
+    const float hi = (float)v;
+    th[i] = make_float2(hi, (float)(v - (double)hi));
+  }
+}
+
+// Writes the first n (0..M) of M fp16 values, packed two per word in w, to
+// dst: 16-byte stores for a whole aligned run, else 4-byte stores where dst is
+// 4-byte aligned, else 2-byte stores.
+template <int M>
+__device__ __forceinline__ void store_run(uint16_t *dst, const uint32_t (&w)[M / 2], int n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+  if (n == M && (a & 15u) == 0) {
+#pragma unroll
+    for (int k = 0; k < M / 8; ++k)
+      reinterpret_cast<uint4 *>(dst)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  } else if ((a & 3u) == 0) {
+#pragma unroll
+    for (int m = 0; m < M / 2; ++m) {
+      if (2 * m + 2 <= n) reinterpret_cast<uint32_t *>(dst)[m] = w[m];
+      else if (2 * m < n) dst[2 * m] = (uint16_t)(w[m] & 0xFFFFu);
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < M / 2; ++m) {
+      if (2 * m < n) dst[2 * m] = (uint16_t)(w[m] & 0xFFFFu);
+      if (2 * m + 1 < n) dst[2 * m + 1] = (uint16_t)(w[m] >> 16);
+    }
+  }
+}
+
 constexpr int XST = 2;      // x staging stages
 constexpr int ST = 3;       // A/B operand stages
 constexpr int NCONV = 8;    // converter / epilogue warps
@@ -34,6 +97,9 @@ constexpr int THREADS = (2 + NCONV) * 32;
 
 struct QkvArgs {
   int C, N, h, dp, ldq, ldn, BN, nk, tmem_cols, xbytes;
+  int d, inter;              // head dim; Q/K rows pair-interleaved (then d == dp, d % 16 == 0)
+  int rope;                  // rotate Q and K in the epilogue (needs inter)
+  uint32_t stall;            // test hook: the producer stops after this many loads (0: never)
   const float *ga;
   const float *gs;
   const float *bias;
@@ -129,6 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
         const int sx = kb % XST, s = kb % ST;
+        if (args.stall && (uint32_t)(nx + nb) >= args.stall) break;  // test hook: consumers' waits expire
         if (kb >= XST && !mbar_wait(&x_empty[sx], ((kb / XST) - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(&x_full[sx], (uint32_t)args.xbytes);
         tma_load_3d(sm + L.xs + sx * args.xbytes, &xmap, &x_full[sx], p0, kb * BK, b);
@@ -140,9 +207,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Never leave with a copy in flight.
       for (int kb = (nx > XST ? nx - XST : 0); kb < nx; ++kb)
-        mbar_wait_drain(&x_full[kb % XST], (kb / XST) & 1, ab.limit_ns);
+        mbar_wait_drain(&x_full[kb % XST], (kb / XST) & 1, drain_limit(ab));
       for (int kb = (nb > ST ? nb - ST : 0); kb < nb; ++kb)
-        mbar_wait_drain(&b_full[kb % ST], (kb / ST) & 1, ab.limit_ns);
+        mbar_wait_drain(&b_full[kb % ST], (kb / ST) & 1, drain_limit(ab));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -174,10 +241,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (elect_one()) mma_commit(acc_full);
         __syncwarp();
       }
-      if (!ok && issued) {
+      if (issued) {  // every issued MMA completes before tensor memory is freed
         if (elect_one()) mma_commit(drain);
         __syncwarp();
-        mbar_wait_drain(drain, 0, ab.limit_ns);
+        mbar_wait_drain(drain, 0, drain_limit(ab));
       }
     }
     __syncwarp();
@@ -240,7 +307,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // order, one 4 KB chunk per 16 features: Q/K chunks as [128 pixels][16]
     // (rows of the q/k layout), V chunks as [16][128 pixels] (rows of the
     // transposed v layout).  One thread then stores each chunk with TMA,
-    // which clips pixels past N.
+    // which clips pixels past N.  With pair-interleaved Q/K rows a chunk holds
+    // 8 pairs (features i0..i0+7 and d/2+i0..d/2+i0+7): it is staged as two
+    // [128 pixels][8] halves, rotated first when the rotary embedding is on.
+    float2 *th = reinterpret_cast<float2 *>(sm + L.slot);  // rotation thetas (the x staging slots are idle now)
+    if (args.rope) {
+      named_bar_sync(1, NCONV * 32);  // every converter is done with its slot
+      rope_thetas(th, args.d, threadIdx.x - 64, NCONV * 32);
+      named_bar_sync(1, NCONV * 32);
+    }
     if (ok && mbar_wait_warp(acc_full, 0, ab)) {
       __syncwarp();
       tc_fence_after();
@@ -259,7 +334,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + __ldg(args.bias + f0 + i);
         uint8_t *chunk = stage + c16 * 4096;
-        if (sec < 2) {
+        if (sec < 2 && args.inter) {
+          if (args.rope) {
+            const int i0 = (f0 % args.dp) >> 1;
+            const float t = (float)(p0 + row);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rope_pair(v[2 * j], v[2 * j + 1], t, th[i0 + j]);
+          }
+          uint4 wx, wy;
+          wx.x = pack_half2(v[0], v[2]); wx.y = pack_half2(v[4], v[6]);
+          wx.z = pack_half2(v[8], v[10]); wx.w = pack_half2(v[12], v[14]);
+          wy.x = pack_half2(v[1], v[3]); wy.y = pack_half2(v[5], v[7]);
+          wy.z = pack_half2(v[9], v[11]); wy.w = pack_half2(v[13], v[15]);
+          reinterpret_cast<uint4 *>(chunk)[row] = wx;
+          reinterpret_cast<uint4 *>(chunk + 2048)[row] = wy;
+        } else if (sec < 2) {
           uint4 w0, w1;
           w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
           w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
@@ -284,7 +373,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int e0 = f0 % args.dp;
           const int bh = b * args.h + hd;
           const uint8_t *chunk = stage + c16 * 4096;
-          if (sec == 0) tma_store_3d(&qmap, chunk, e0, p0, bh);
+          if (sec < 2 && args.inter) {
+            // two 8-feature halves: features i0.. and d/2 + i0..
+            const CUtensorMap *m = sec == 0 ? &qmap : &kmap;
+            tma_store_3d(m, chunk, e0 >> 1, p0, bh);
+            tma_store_3d(m, chunk + 2048, args.d / 2 + (e0 >> 1), p0, bh);
+          } else if (sec == 0) tma_store_3d(&qmap, chunk, e0, p0, bh);
           else if (sec == 1) tma_store_3d(&kmap, chunk, e0, p0, bh);
           else tma_store_3d(&vmap, chunk, p0, e0, bh);
         }
@@ -319,8 +413,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 //                [BN][64] k-blocks per 32 KB slot
 //   warp 1       MMA warp (warp-uniform loop, elected lane issues)
 //   warps 2..9   converters (x block -> A columns in tensor memory), then
-//                epilogues (bias, fp16, direct stores into Q/K rows and V^T
-//                rows)
+//                epilogues (bias, the optional rotary embedding, fp16; Q/K
+//                rows stored directly, V^T staged in shared memory and
+//                written by TMA)
 constexpr int RNST = 6;                  // ring slots of 32 KB
 constexpr int RSLOT = 32768;
 constexpr int RTHREADS = 352;
@@ -329,6 +424,10 @@ constexpr uint32_t RA_COL = 256;         // A operand: tensor-memory columns 256
 struct ResArgs {
   int C, N, h, dp, ldq, ldn, BN, nkb, nslices, spg, xbytes;
   int w3d;  // weights as one 3-D box of two 64-channel chunks per slot (C % 64 == 0), else two 2-D boxes
+  int cw;   // epilogue chunk: 32 columns (dp % 32 == 0 and BN % 64 == 0) or 16
+  int d, inter;        // head dim; Q/K rows pair-interleaved (qk_pair_interleaved)
+  int rope;            // rotate Q and K in the epilogue (needs inter)
+  uint32_t stall;      // test hook: each producer stops at this load index (0: never)
   const float *ga;
   const float *gs;
   const float *bias;
@@ -340,14 +439,160 @@ struct ResArgs {
 };
 // barriers: full[RNST], empty[RNST], xfree[RNST], a_ready, acc_full[2], acc_empty[2], drain
 constexpr int RNBARS = 3 * RNST + 6;
-constexpr uint32_t RES_SLOT_OFF = RNST * RSLOT;              // converters' GN scale/shift staging
+constexpr uint32_t RES_VST_OFF = RNST * RSLOT;               // V^T staging: 4 KB per epilogue warp
+constexpr uint32_t RES_SLOT_OFF = RES_VST_OFF + 32768;       // converters' GN scale/shift staging
 constexpr uint32_t RES_BARS_OFF = RES_SLOT_OFF + NCONV * 256;
 constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
+
+// One chunk of CW accumulator columns of a slice, for the lanes' 32 pixels:
+// bias, then by section
+//   Q/K, pair-interleaved: pairs (x = feature i, y = feature i + d/2),
+//        rotated when the table is given, written back to their own
+//        features (two pieces per row; rows >= d of the packed head are the
+//        zero padding [d, dp));
+//   Q/K, plain order: the chunk's features as one piece per row;
+//   V:   into the warp's V^T staging area [CW features][32 pixels] at vst.
+// Q/K rows go straight to global memory; with CW = 32 a 4 x 4 shuffle
+// transpose inside each group of 4 lanes makes lanes 4g..4g+3 write the four
+// 16-byte pieces of one row per store instruction.
+template <int CW>
+__device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t taddr, int F0, int b, int p0, int q4,
+                                              int lane, uint8_t *vst, const float2 *th) {
+  uint32_t r[CW];
+  if constexpr (CW == 32) tmem_ld32(taddr, r);
+  else tmem_ld16(taddr, r);
+  // The chunk's biases, the same for every lane (broadcast vector loads).
+  float bv[CW];
+  const float4 *bq = reinterpret_cast<const float4 *>(args.bias + F0);
+#pragma unroll
+  for (int k = 0; k < CW / 4; ++k) {
+    const float4 t4 = __ldg(bq + k);
+    bv[4 * k] = t4.x;
+    bv[4 * k + 1] = t4.y;
+    bv[4 * k + 2] = t4.z;
+    bv[4 * k + 3] = t4.w;
+  }
+  tmem_wait_ld();
+  float v[CW];
+#pragma unroll
+  for (int k = 0; k < CW; ++k) v[k] = __uint_as_float(r[k]) + bv[k];
+  const int hdp = args.h * args.dp;
+  const int sec = F0 / hdp;
+  const int hd = (F0 / args.dp) % args.h;
+  const int r0 = F0 % args.dp;  // packed row of the chunk's first column inside its head
+  const int row = q4 * 32 + lane;
+  const int pix = p0 + row;
+  if (sec == 2) {
+    // this warp's V^T staging: [CW features][32 pixels], 64-byte rows
+    __half *st = reinterpret_cast<__half *>(vst);
+#pragma unroll
+    for (int k = 0; k < CW; ++k) st[k * 32 + lane] = __float2half_rn(v[k]);
+    return;
+  }
+  const long long bh = (long long)b * args.h + hd;
+  uint16_t *qk = (sec == 0 ? args.q : args.k) + bh * args.N * args.ldq;
+  const int j4 = lane & 3, g4 = lane & ~3;
+  if (args.inter) {
+    const int hd2 = args.d >> 1;
+    const int i0 = r0 >> 1;
+    const int npair = max(0, min(hd2 - i0, CW / 2));  // pairs of this chunk
+    if (args.rope) {
+      const float t = (float)pix;
+#pragma unroll
+      for (int j = 0; j < CW / 2; ++j)
+        if (j < npair) rope_pair(v[2 * j], v[2 * j + 1], t, th[i0 + j]);
+    }
+    if (CW == 32 && npair == 16 && (hd2 & 7) == 0) {
+      // four 16-byte pieces per row: x features i0.., i0+8..; y features d/2+i0.., d/2+i0+8..
+      uint32_t a[4][4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int j = 8 * k + 2 * m;
+          a[k][m] = pack_half2(v[2 * j], v[2 * j + 2]);
+          a[2 + k][m] = pack_half2(v[2 * j + 1], v[2 * j + 3]);
+        }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        // transpose the 4 x 4 matrix (lane j of the group, piece k) -> (lane k, piece j)
+        const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
+        const uint32_t s1 = (j4 & 1) ? a[2][m] : a[3][m];
+        const uint32_t t0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+        const uint32_t t1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+        if (j4 & 1) { a[0][m] = t0; a[2][m] = t1; } else { a[1][m] = t0; a[3][m] = t1; }
+        const uint32_t u0 = (j4 & 2) ? a[0][m] : a[2][m];
+        const uint32_t u1 = (j4 & 2) ? a[1][m] : a[3][m];
+        const uint32_t w0 = __shfl_xor_sync(0xFFFFFFFFu, u0, 2);
+        const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, u1, 2);
+        if (j4 & 2) { a[0][m] = w0; a[1][m] = w1; } else { a[2][m] = w0; a[3][m] = w1; }
+      }
+      const int f = (j4 < 2) ? i0 + 8 * j4 : hd2 + i0 + 8 * (j4 - 2);
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int rp = p0 + q4 * 32 + g4 + ii;  // row written by this group in store ii
+        if (rp < args.N)
+          *reinterpret_cast<uint4 *>(qk + (long long)rp * args.ldq + f) = make_uint4(a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
+      }
+      return;
+    }
+    if (pix >= args.N) return;
+    uint16_t *dst = qk + (long long)pix * args.ldq;
+    uint32_t xw[CW / 4], yw[CW / 4];
+#pragma unroll
+    for (int m = 0; m < CW / 4; ++m) {
+      xw[m] = pack_half2(v[4 * m], v[4 * m + 2]);
+      yw[m] = pack_half2(v[4 * m + 1], v[4 * m + 3]);
+    }
+    store_run<CW / 2>(dst + i0, xw, npair);
+    store_run<CW / 2>(dst + hd2 + i0, yw, npair);
+    // packed rows [d, dp) are the head's zero padding, in place
+    for (int f = max(r0, args.d); f < min(r0 + CW, args.dp); ++f) dst[f] = 0;
+    return;
+  }
+  if constexpr (CW == 32) {
+    uint32_t a[4][4];  // a[k] = this row's 16-byte piece k (features 8k .. 8k+7)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
+      const uint32_t s1 = (j4 & 1) ? a[2][m] : a[3][m];
+      const uint32_t t0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+      const uint32_t t1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+      if (j4 & 1) { a[0][m] = t0; a[2][m] = t1; } else { a[1][m] = t0; a[3][m] = t1; }
+      const uint32_t u0 = (j4 & 2) ? a[0][m] : a[2][m];
+      const uint32_t u1 = (j4 & 2) ? a[1][m] : a[3][m];
+      const uint32_t w0 = __shfl_xor_sync(0xFFFFFFFFu, u0, 2);
+      const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, u1, 2);
+      if (j4 & 2) { a[0][m] = w0; a[1][m] = w1; } else { a[2][m] = w0; a[3][m] = w1; }
+    }
+    uint16_t *base = qk + r0 + j4 * 8;
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const int rp = p0 + q4 * 32 + g4 + ii;
+      if (rp < args.N)
+        *reinterpret_cast<uint4 *>(base + (long long)rp * args.ldq) = make_uint4(a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
+    }
+  } else {
+    if (pix >= args.N) return;
+    uint16_t *dst = qk + (long long)pix * args.ldq + r0;
+    uint4 w0, w1;
+    w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
+    w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
+    w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
+    w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
+    reinterpret_cast<uint4 *>(dst)[0] = w0;
+    reinterpret_cast<uint4 *>(dst)[1] = w1;
+  }
+}
 
 template <int DT>
 __global__ void __launch_bounds__(RTHREADS, 1)
     qkv_resident_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                        const ResArgs args) {
+                        const __grid_constant__ CUtensorMap vmap, const ResArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
   // The layout needs a 1024-byte aligned base (128B-swizzled operands) and
@@ -400,6 +645,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&xmap);
     tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&vmap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -422,7 +668,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     if (lane == 0) {
       const int me = warp == 0 ? 0 : 1;
       int last = -1;
+      bool stalled = false;
       for (int t = me; t < nloads; t += 2) {
+        if (args.stall && (uint32_t)t >= args.stall) { stalled = true; break; }  // test hook
         const int s = t % RNST;
         const int prev = t - RNST;
         if (prev >= 0) {
@@ -455,9 +703,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         }
         last = t;
       }
-      if (*abort_flag)
+      if (*abort_flag || stalled)
         for (int t = last; t >= 0 && t > last - 2 * RNST; t -= 2)
-          mbar_wait_drain(&full[t % RNST], (uint32_t)((t / RNST) & 1), ab.limit_ns);
+          mbar_wait_drain(&full[t % RNST], (uint32_t)((t / RNST) & 1), drain_limit(ab));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -496,10 +744,10 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         __syncwarp();
       }
     }
-    if (!ok && issued) {
+    if (issued) {  // every issued MMA completes before tensor memory is freed
       if (elect_one()) mma_commit(drain);
       __syncwarp();
-      mbar_wait_drain(drain, 0, ab.limit_ns);
+      mbar_wait_drain(drain, 0, drain_limit(ab));
     }
     __syncwarp();
   } else {
@@ -545,129 +793,73 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       if (lane == 0) mbar_arrive(&xfree[s]);  // the x block has been read
       tmem_st16(lane_base + RA_COL + (uint32_t)(kb * 32 + hc * 16), w);
     }
+    tmem_wait_st();  // also after an abort: no store may be pending when tensor memory is freed
     if (ok) {
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(a_ready);
     }
     // ------------------------------------------------------------ epilogues
+    // Each warp stages its own V^T pieces ([CW features][32 pixels] per chunk,
+    // 4 KB per warp and slice) and writes them with its own TMA stores, so the
+    // eight warps never wait for one another; before refilling its staging a
+    // warp waits until its previous stores have read it.
+    uint8_t *vst = sm + RES_VST_OFF + cw * 4096;
+    bool stores_pending = false;
+    // Rotation thetas in the converters' (now idle) scale/shift slots.  Every
+    // epilogue warp takes both barriers, whatever its state.
+    float2 *th = reinterpret_cast<float2 *>(sm + RES_SLOT_OFF);
+    if (args.rope) {
+      named_bar_sync(1, NCONV * 32);
+      rope_thetas(th, args.d, cw * 32 + lane, NCONV * 32);
+      named_bar_sync(1, NCONV * 32);
+    }
     const int hdp = args.h * args.dp;
-    const int pix = p0 + px;
+    const int nch = args.BN / args.cw;
     for (int i = 0; i < nsl && ok; ++i) {
       const int buf = i & 1;
       if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
       const int fs = (sl0 + (i + rot) % nsl) * args.BN;
-      const int ncol = args.BN / 2;
-      if (args.dp % 32 == 0 && ncol % 32 == 0) {
-        // Warp (q4, hc) takes columns [hc * BN/2, (hc+1) * BN/2) of the slice,
-        // 32 at a time (never straddling a head or section when dp % 32 == 0).
-        // Q/K rows are written 64 contiguous bytes per row: a 4 x 4 shuffle
-        // transpose inside each group of 4 lanes makes lanes 4g..4g+3 write
-        // the four 16-byte pieces of one row per store instruction.
-        const int cbase = hc * ncol;
-        const int j4 = lane & 3, g4 = lane & ~3;
-        // Section, head and offset of the first chunk; later chunks advance
-        // by 32 features (a chunk never straddles a head when dp % 32 == 0).
-        int sec = (fs + cbase) / hdp;
-        int hd = ((fs + cbase) / args.dp) % args.h;
-        int e0 = (fs + cbase) % args.dp;
-        for (int c32 = 0; c32 < ncol; c32 += 32) {
-          const int f0 = fs + cbase + c32;
-          uint32_t r[32];
-          tmem_ld32(lane_base + (uint32_t)(buf * 128 + cbase + c32), r);
-          // The chunk's 32 biases, the same for every lane (broadcast loads).
-          const float4 *bq = reinterpret_cast<const float4 *>(args.bias + f0);
-          float bv[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 t4 = __ldg(bq + k);
-            bv[4 * k] = t4.x;
-            bv[4 * k + 1] = t4.y;
-            bv[4 * k + 2] = t4.z;
-            bv[4 * k + 3] = t4.w;
-          }
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) + bv[k];
-          const long long bh = (long long)b * args.h + hd;
-          if (sec < 2) {
-            uint32_t a[4][4];  // a[k] = this row's 16-byte piece k (features 8k .. 8k+7)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-              for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              // transpose the 4 x 4 matrix (lane j of the group, piece k) -> (lane k, piece j)
-              const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
-              const uint32_t s1 = (j4 & 1) ? a[2][m] : a[3][m];
-              const uint32_t t0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
-              const uint32_t t1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
-              if (j4 & 1) { a[0][m] = t0; a[2][m] = t1; } else { a[1][m] = t0; a[3][m] = t1; }
-              const uint32_t u0 = (j4 & 2) ? a[0][m] : a[2][m];
-              const uint32_t u1 = (j4 & 2) ? a[1][m] : a[3][m];
-              const uint32_t w0 = __shfl_xor_sync(0xFFFFFFFFu, u0, 2);
-              const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, u1, 2);
-              if (j4 & 2) { a[0][m] = w0; a[1][m] = w1; } else { a[2][m] = w0; a[3][m] = w1; }
+      const bool has_v = fs + args.BN > 2 * hdp;
+      if (has_v && stores_pending) {
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+      }
+      const uint32_t acc = lane_base + (uint32_t)(buf * 128);
+      int nv = 0;  // V chunks staged by this warp in this slice
+      for (int c = hc; c < nch; c += 2) {
+        const int F0 = fs + c * args.cw;
+        uint8_t *vs = vst + nv * args.cw * 64;
+        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), F0, b, p0, q4, lane, vs, th);
+        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), F0, b, p0, q4, lane, vs, th);
+        if (F0 >= 2 * hdp) ++nv;
+      }
+      if (nv > 0) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          int k = 0;
+          for (int c = hc; c < nch; c += 2) {
+            const int F0 = fs + c * args.cw;
+            if (F0 < 2 * hdp) continue;
+            for (int u = 0; u < args.cw / 16; ++u) {
+              const int F = F0 + 16 * u;
+              tma_store_3d(&vmap, vst + (k * args.cw + 16 * u) * 64, p0 + q4 * 32, F % args.dp,
+                           b * args.h + (F / args.dp) % args.h);
             }
-            uint16_t *base = (sec == 0 ? args.q : args.k) + bh * args.N * args.ldq + e0 + j4 * 8;
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-              const int rp = p0 + q4 * 32 + g4 + ii;  // row written by this group in store ii
-              if (rp < args.N)
-                *reinterpret_cast<uint4 *>(base + (long long)rp * args.ldq) = make_uint4(a[ii][0], a[ii][1], a[ii][2], a[ii][3]);
-            }
-          } else if (pix < args.N) {
-            __half *dst = reinterpret_cast<__half *>(args.vt) + (bh * args.dp + e0) * args.ldn + pix;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) dst[(long long)k * args.ldn] = __float2half_rn(v[k]);
+            ++k;
           }
-          e0 += 32;
-          if (e0 == args.dp) {
-            e0 = 0;
-            if (++hd == args.h) {
-              hd = 0;
-              ++sec;
-            }
-          }
+          tma_store_commit();
         }
-      } else {
-        for (int c16 = hc; c16 < args.BN / 16; c16 += 2) {
-          uint32_t r[16];
-          tmem_ld16(lane_base + (uint32_t)(buf * 128 + c16 * 16), r);
-          tmem_wait_ld();
-          const int f0 = fs + c16 * 16;
-          const int sec = f0 / hdp;
-          const int hd = (f0 / args.dp) % args.h;
-          const int e0 = f0 % args.dp;
-          const long long bh = (long long)b * args.h + hd;
-          float v[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]) + __ldg(args.bias + f0 + k);
-          if (pix >= args.N) continue;
-          if (sec < 2) {
-            uint16_t *dst = (sec == 0 ? args.q : args.k) + (bh * args.N + pix) * args.ldq + e0;
-            uint4 w0, w1;
-            w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
-            w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
-            w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
-            w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
-            reinterpret_cast<uint4 *>(dst)[0] = w0;
-            reinterpret_cast<uint4 *>(dst)[1] = w1;
-          } else {
-            __half *dst = reinterpret_cast<__half *>(args.vt) + (bh * args.dp + e0) * args.ldn + pix;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) dst[(long long)k * args.ldn] = __float2half_rn(v[k]);
-          }
-        }
+        stores_pending = true;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    if (stores_pending && lane == 0) tma_store_wait_all();
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -679,6 +871,15 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   }
 }
 
+// The resident-tile kernel serves C <= 512 (the A tile fits tensor-memory
+// columns 256..511) when the device grants its shared memory.
+bool resident_ok(const Dims &dm) {
+  int max_smem = 232448, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return (dm.C + BK - 1) / BK <= 8 && (int)RES_SMEM <= max_smem;
+}
+
 int pick_bn(int ntot) {
   for (int bn = 256; bn >= 16; bn -= 16)
     if (ntot % bn == 0) return bn;
@@ -687,10 +888,17 @@ int pick_bn(int ntot) {
 
 }  // namespace
 
+bool qk_pair_interleaved(const Dims &dm) {
+  if (dm.h <= 0 || dm.d % 16) return false;
+  return resident_ok(dm) || dm.dp == dm.d;
+}
+
 int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const float *ga, const float *gs,
                     const uint16_t *w_qkv, const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt,
-                    const KParams &kp, cudaStream_t st) {
+                    const KParams &kp, cudaStream_t st, int rope) {
   const int es = dtype == 0 ? 4 : 2;
+  const int inter = qk_pair_interleaved(dm) ? 1 : 0;
+  if (rope && !inter) return 2;  // the fused rotation needs pair-interleaved Q/K rows
   CUtensorMap xmap, wmap;
   {
     const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.C, (uint64_t)dm.B};
@@ -714,7 +922,8 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     const uint64_t BH = (uint64_t)dm.B * dm.h;
     const uint64_t dims[3] = {(uint64_t)dm.ldq, (uint64_t)dm.N, BH};
     const uint64_t strides[2] = {(uint64_t)dm.ldq * 2, (uint64_t)dm.N * dm.ldq * 2};
-    const uint32_t box[3] = {16, BM, 1};
+    // pair-interleaved rows leave the general kernel as 8-feature halves
+    const uint32_t box[3] = {(uint32_t)((inter && !resident_ok(dm)) ? 8 : 16), BM, 1};
     if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return 1;
@@ -729,9 +938,8 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
       return 1;
   }
   const int nkb = (dm.C + BK - 1) / BK;
-  int max_smem = 232448, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
   // Resident tile: A (C/2 columns) must fit tensor-memory columns 256..511,
   // a slice (BN <= 128 features) one 128-column accumulator.
   int BNr = 0;
@@ -740,8 +948,17 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
       BNr = bn;
       break;
     }
-  if (nkb <= 8 && BNr > 0 && BM * BK * es <= RSLOT && (int)RES_SMEM <= max_smem) {
-    CUtensorMap wmap_r;
+  if (resident_ok(dm) && BNr > 0 && BM * BK * es <= RSLOT) {
+    CUtensorMap wmap_r, vmap_r;
+    {
+      // V^T pieces of one epilogue warp: [16 features][32 pixels]
+      const uint64_t vdims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, (uint64_t)dm.B * dm.h};
+      const uint64_t vstrides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
+      const uint32_t vbox[3] = {32, 16, 1};
+      if (encode_tiled(&vmap_r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, vdims, vstrides, vbox,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return 1;
+    }
     const int w3d = (dm.C % BK == 0) ? 1 : 0;
     if (w3d) {
       // W viewed as [64-channel chunk][feature][64 channels]: one box = two
@@ -774,21 +991,28 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     ResArgs r{};
     r.C = dm.C; r.N = dm.N; r.h = dm.h; r.dp = dm.dp; r.ldq = dm.ldq; r.ldn = dm.ldn; r.BN = BNr;
     r.nkb = nkb; r.nslices = nslices; r.spg = spg; r.xbytes = BM * BK * es; r.w3d = w3d;
+    r.cw = (dm.dp % 32 == 0 && BNr % 64 == 0) ? 32 : 16;
+    r.d = dm.d; r.inter = inter; r.rope = rope ? 1 : 0; r.stall = stall_for(kp, STALL_QKV);
     r.ga = ga; r.gs = gs; r.bias = b_qkv; r.q = q; r.k = k; r.vt = vt;
     r.err = kp.err; r.timeout_ns = kp.timeout_ns;
     const uint32_t smem = RES_SMEM;
     const dim3 grid(ng, (dm.N + BM - 1) / BM, dm.B);
     if (dtype == 0) {
       cudaFuncSetAttribute(qkv_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
+      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, vmap_r, r);
     } else {
       cudaFuncSetAttribute(qkv_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
+      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, vmap_r, r);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
+  // Here pair-interleaved rows always mean d == dp and d % 16 == 0
+  // (qk_pair_interleaved), so every 16-feature chunk holds 8 whole pairs and
+  // both of its 8-feature halves start 16-byte aligned.
+  if (inter && !(dm.dp == dm.d && dm.d % 16 == 0)) return 2;
   QkvArgs a{};
   a.C = dm.C; a.N = dm.N; a.h = dm.h; a.dp = dm.dp; a.ldq = dm.ldq; a.ldn = dm.ldn; a.BN = BN;
+  a.d = dm.d; a.inter = inter; a.rope = rope ? 1 : 0; a.stall = stall_for(kp, STALL_QKV);
   a.nk = (dm.C + BK - 1) / BK;
   a.tmem_cols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
   a.xbytes = BM * BK * es;

@@ -27,6 +27,7 @@ constexpr int kMaxDevices = 64;
 thread_local char t_err[512] = "";
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_split_policy{0};
+std::atomic<uint32_t> g_stall_mask{0}, g_stall_after{0};
 std::mutex g_mu;
 uint32_t *g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
@@ -79,6 +80,8 @@ ssa_status kparams(KParams *kp, int *num_sms) {
   if (s != SSA_OK) return s;
   kp->err = err;
   kp->timeout_ns = g_timeout_ns.load();
+  kp->stall_mask = g_stall_mask.load();
+  kp->stall_after = g_stall_after.load();
   return SSA_OK;
 }
 
@@ -196,8 +199,11 @@ ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, con
   uint16_t *k = reinterpret_cast<uint16_t *>(ws + wl.k);
   uint16_t *vt = reinterpret_cast<uint16_t *>(ws + wl.vt);
   uint16_t *o = reinterpret_cast<uint16_t *>(ws + wl.o);
-  cudaError_t e = launch_gn_stats(x, dm.B, dm.C, dm.N, dm.G, (int)dt, p.gw, p.gb, nullptr, nullptr, ga, gs,
-                                  num_sms, st);
+  // The rotary embedding runs inside the projection's epilogue when Q/K rows
+  // are pair-interleaved; with the query-key norm (which must come first) it
+  // stays a separate pass after the norm.
+  const bool fuse_rope = var.rope && !var.q_gamma && qk_pair_interleaved(dm);
+  cudaError_t e = launch_gn_stats(x, dm.B, dm.C, dm.N, dm.G, (int)dt, p.gw, p.gb, nullptr, nullptr, ga, gs, num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "gn_stats launch");
   const void *xq = x;
   int ldx = x_pitch(dm.N, dt);
@@ -206,14 +212,14 @@ ssa_status run_block(const Dims &dm, ssa_dtype dt, const void *x, void *out, con
     if (e != cudaSuccess) return cuda_fail(e, "pad_x launch");
     xq = ws + wl.xpad;
   }
-  int r = launch_qkv_gemm(dm, (int)dt, xq, ldx, ga, gs, w_qkv, b_qkv, q, k, vt, kp, st);
+  int r = launch_qkv_gemm(dm, (int)dt, xq, ldx, ga, gs, w_qkv, b_qkv, q, k, vt, kp, st, fuse_rope ? 1 : 0);
   if (r == 1) return fail(SSA_ERR_CUDA, "qkv_gemm: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "qkv_gemm launch");
   if (var.q_gamma) {
     e = launch_qk_norm(dm, (int)dt, q, k, var.q_gamma, var.k_gamma, st);
     if (e != cudaSuccess) return cuda_fail(e, "qk norm launch");
   }
-  if (var.rope) {
+  if (var.rope && !fuse_rope) {
     e = launch_rope(dm, q, k, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope launch");
   }
@@ -287,6 +293,11 @@ extern "C" {
 const char *ssa_last_error_string(void) { return t_err; }
 
 void ssa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void ssa_debug_set_producer_stall(uint32_t kernel_mask, uint32_t after_loads) {
+  g_stall_mask.store(after_loads ? (kernel_mask & 7u) : 0u);
+  g_stall_after.store(after_loads);
+}
 
 ssa_status ssa_set_attention_split(int policy) {
   if (policy < SSA_SPLIT_AUTO || policy > SSA_SPLIT_NEVER)
@@ -523,6 +534,33 @@ ssa_status ssa_qkv_project(const void *x, int B, int C, int H, int W, int num_he
   const Dims dm = make_dims(B, C, H, W, 1, num_heads);
   const int r = launch_qkv_gemm(dm, (int)dtype, x, dm.N, gn_scale, gn_shift, w_qkv, b_qkv, q, k, vt, kp,
                                 static_cast<cudaStream_t>(stream));
+  if (r == 1) return fail(SSA_ERR_CUDA, "qkv_gemm: tensor map encoding failed");
+  if (r) return cuda_fail(cudaGetLastError(), "qkv_gemm launch");
+  return SSA_OK;
+}
+
+ssa_status ssa_qkv_project_rope(const void *x, int B, int C, int H, int W, int num_heads, ssa_dtype dtype,
+                                const float *gn_scale, const float *gn_shift, const uint16_t *w_qkv,
+                                const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt, void *stream) {
+  if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
+  ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s != SSA_OK) return s;
+  if ((s = check_dtype(dtype)) != SSA_OK) return s;
+  if (!x || !gn_scale || !gn_shift || !w_qkv || !b_qkv || !q || !k || !vt)
+    return fail(SSA_ERR_NULL, "a required pointer is NULL");
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q) || !aligned16(k) || !aligned16(vt))
+    return fail(SSA_ERR_ALIGNMENT, "x, w_qkv, q, k and vt must be 16-byte aligned");
+  if (x_pitch(H * W, dtype) != H * W)
+    return fail(SSA_ERR_ALIGNMENT, "H*W*sizeof(x) must be a multiple of 16 bytes for this entry point");
+  const Dims dm = make_dims(B, C, H, W, 1, num_heads);
+  if (dm.d % 2) return fail(SSA_ERR_CONSTRAINT, "rope needs an even head dim (d = %d)", dm.d);
+  if (!qk_pair_interleaved(dm))
+    return fail(SSA_ERR_UNSUPPORTED, "this shape packs Q/K in plain order; rotate with ssa_rope after ssa_qkv_project");
+  KParams kp{};
+  int num_sms = 0;
+  if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
+  const int r = launch_qkv_gemm(dm, (int)dtype, x, dm.N, gn_scale, gn_shift, w_qkv, b_qkv, q, k, vt, kp,
+                                static_cast<cudaStream_t>(stream), 1);
   if (r == 1) return fail(SSA_ERR_CUDA, "qkv_gemm: tensor map encoding failed");
   if (r) return cuda_fail(cudaGetLastError(), "qkv_gemm launch");
   return SSA_OK;

@@ -24,7 +24,10 @@
  *    raised on the device (a bounded wait that expired) are latched in a
  *    device flag and returned by ssa_get_device_status().
  *  - The 16-bit tensor-core operand type is fp16 (fp32 accumulation, fp32
- *    softmax statistics).
+ *    softmax statistics).  Parameters and the projected Q, K, V must lie in
+ *    fp16's range: magnitudes above 65504 become infinite and values below
+ *    2^-24 become zero, without a status (GroupNorm keeps Z near unit scale,
+ *    so this concerns parameters of extreme magnitude only).
  */
 #ifndef SSA_H
 #define SSA_H
@@ -130,11 +133,24 @@ ssa_status ssa_forward_static(const void *x, int B, int C, int H, int W, int num
  *   ldq = dp rounded up to 64,  ldn = N rounded up to 8,  ldc = C rounded up to 8.
  * Layouts (fp16 unless stated):
  *   mean, rstd   [B][G] fp32           gn_scale, gn_shift [B][C] fp32
- *   w_qkv        [3][h][dp][ldc]       rows q|k|v, head-major, zero rows past d
- *   b_qkv        [3][h][dp] fp32       zero past d
+ *   w_qkv        [3][h][dp][ldc]       rows q|k|v, head-major, zero rows past d;
+ *                                      for an even d the q and k rows of a head
+ *                                      may be pair-interleaved (row 2i = feature
+ *                                      i, row 2i+1 = feature i + d/2) so that the
+ *                                      projection can apply the rotary embedding
+ *                                      in its epilogue -- produced and read only
+ *                                      by the library, which decides this from
+ *                                      the shape (d % 16 == 0, and C <= 512 or
+ *                                      d == dp); q and k below keep the plain
+ *                                      feature order either way
+ *   b_qkv        [3][h][dp] fp32       zero past d, same row order as w_qkv, except
+ *                                      that the v bias of padded feature d is 1
  *   w_o          [C][ldc]              b_o [C] fp32
  *   q, k         [B][h][N][ldq]        columns >= dp unspecified
- *   vt           [B][h][dp][ldn]       V transposed per head; columns >= N unspecified
+ *   vt           [B][h][dp][ldn]       V transposed per head; columns >= N unspecified;
+ *                                      when d < dp row d holds ones (the attention
+ *                                      kernels read the softmax row sums from it;
+ *                                      ssa_qkv_project writes it), rows past d+1 zero
  *   o            [B][N][ldc]           heads concatenated along channels
  */
 
@@ -164,6 +180,20 @@ ssa_status ssa_qkv_project(const void *x, int B, int C, int H, int W, int num_he
                            const float *gn_scale, const float *gn_shift,
                            const uint16_t *w_qkv, const float *b_qkv,
                            uint16_t *q, uint16_t *k, uint16_t *vt, void *stream);
+
+/* ssa_qkv_project with the rotary embedding of the variants (HNDL attention
+ * operator page, Rotary embeddings paragraph: rotate-half over the head dim,
+ * base 10000) applied to Q and K in the projection's epilogue, before their
+ * single rounding to fp16.  The angle t * 10000^(-2i/d) is formed from an
+ * fp64 frequency (two fp32 parts) and reduced to [-pi, pi] before cos/sin,
+ * so it is exact to about 1e-6 rad at every position.  SSA_ERR_CONSTRAINT for
+ * an odd head dim; SSA_ERR_UNSUPPORTED for shapes whose Q/K rows are packed in
+ * plain order (head dims that are not a multiple of 16; there:
+ * ssa_qkv_project, then ssa_rope). */
+ssa_status ssa_qkv_project_rope(const void *x, int B, int C, int H, int W, int num_heads, ssa_dtype dtype,
+                                const float *gn_scale, const float *gn_shift,
+                                const uint16_t *w_qkv, const float *b_qkv,
+                                uint16_t *q, uint16_t *k, uint16_t *vt, void *stream);
 
 /* O_j = softmax(Q_j K_j^T / sqrt(d)) V_j for every (b, head), never forming
  * the N x N matrix; o receives the heads side by side (layout above). */
@@ -210,8 +240,10 @@ typedef struct ssa_options {
 size_t ssa_workspace_size_ex(int B, int C, int H, int W, int num_groups, int num_heads,
                              ssa_dtype dtype, const ssa_options *opt);
 
-/* ssa_forward with the variants: the rotation runs after the projection (in
- * place on Q and K), the table is packed into the workspace, and the
+/* ssa_forward with the variants: the rotation runs in the projection's
+ * epilogue (or, with the query-key norm, or for shapes whose Q/K rows are
+ * packed in plain order, as a separate pass after it), the table is packed
+ * into the workspace, and the
  * attention kernels add the bias and apply the mask to their logits, skipping
  * key tiles that the causal mask removes entirely. */
 ssa_status ssa_forward_ex(const void *x, int B, int C, int H, int W, int num_groups, int num_heads,
@@ -289,6 +321,21 @@ void ssa_set_wait_timeout_ns(uint64_t ns);
  * bounded by `timeout_ns`; the wait expires, latches SSA_ERR_TIMEOUT and the
  * kernel returns.  Exercises the timeout path without faulting the GPU. */
 ssa_status ssa_debug_timeout_probe(uint64_t timeout_ns, void *stream);
+
+/* Test hook for the device-side timeout path of the block's own kernels.
+ * After this call the TMA producers of the kernels named in kernel_mask
+ * (SSA_STALL_QKV, SSA_STALL_ATTENTION for head dims up to 256,
+ * SSA_STALL_OUT_PROJ) stop after after_loads loads of a launch, as if the
+ * memory system had stalled: their consumers' bounded waits then expire, the
+ * kernel latches SSA_ERR_TIMEOUT, drains its copies and MMAs, frees its tensor
+ * memory and returns, and ssa_get_device_status() reports it.  No fault is
+ * involved.  after_loads = 0 turns the hook off.  Process-wide; applies to
+ * launches after the call.  (Head dim 512 -- the two-CTA cluster kernel -- is
+ * not covered.) */
+#define SSA_STALL_QKV 1u
+#define SSA_STALL_ATTENTION 2u
+#define SSA_STALL_OUT_PROJ 4u
+void ssa_debug_set_producer_stall(uint32_t kernel_mask, uint32_t after_loads);
 
 /* Human-readable detail of the last error returned on this thread. */
 const char *ssa_last_error_string(void);

@@ -291,3 +291,42 @@ def test_pair_split_matches_whole_tiles(ssa, split_policy):
     with pytest.raises(ssa.SsaError) as e:
         ssa.set_attention_split(7)
     assert e.value.status == 1
+
+
+ABORT_CASES = [
+    # name, B, C, H, W, G, h, dtype, kernel whose producer stalls
+    ("qkv-resident", 2, 320, 32, 32, 32, 8, "f32", 1),       # resident QKV (C <= 512), both producer warps
+    ("qkv-general", 2, 768, 8, 16, 32, 12, "bf16", 1),       # QKV for C > 512
+    ("attention-single", 2, 320, 32, 32, 32, 8, "f32", 2),   # single mode (two CTAs per SM), d = 40
+    ("attention-double", 1, 320, 16, 16, 16, 1, "f32", 2),   # double mode (two O halves), d = 320
+    ("out-proj-resident", 2, 320, 64, 64, 32, 8, "f32", 4),  # resident out-projection (C <= 512, >= 64 tiles)
+    ("out-proj-small", 2, 320, 32, 32, 32, 8, "f32", 4),     # out-projection, one tile per CTA (16 tiles)
+    ("out-proj-general", 2, 768, 8, 16, 32, 12, "bf16", 4),  # out-projection for C > 512
+]
+
+
+@pytest.mark.parametrize("case", ABORT_CASES, ids=[c[0] for c in ABORT_CASES])
+def test_stalled_producer_times_out_and_context_survives(ssa, case):
+    """The timeout path of the block's own kernels, without a fault: the test
+    hook stops one kernel's TMA producer after a few loads, so its consumers
+    wait for data that never comes.  With a 1 ms wait limit each wait expires,
+    the kernel latches SSA_ERR_TIMEOUT, drains its copies and MMAs, frees its
+    tensor memory and returns; the next call at the default limit, hook off,
+    matches the oracle."""
+    name, B, C, H, W, G, h, dt, mask = case
+    wl = wls.custom(name, B, C, H, W, G, h, dt, seed=13)
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    try:
+        ssa.ssa_set_wait_timeout_ns(1_000_000)
+        for after in (1, 2, 3):
+            ssa.ssa_debug_set_producer_stall(mask, after)
+            ssa.ssa_forward(xd, pd, G, h)
+            assert ssa.ssa_get_device_status() == 7, (after, ssa.ssa_last_error_string())
+    finally:
+        ssa.ssa_debug_set_producer_stall(0, 0)
+        ssa.ssa_set_wait_timeout_ns(2_000_000_000)
+    out = ssa.ssa_forward(xd, pd, G, h)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    rel, mx = _compare(out, x, p, wl)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)

@@ -5,10 +5,11 @@ the fp64 oracle, through the C ABI (ssa_forward_ex / ssa_forward_planned_ex
 and the step entry points).
 
 Tolerances as for the block (branch relative L2 <= 1e-2, max |delta| of out
-<= 5e-2).  The rotary angles are built in fp32 on the GPU (as the page
-prescribes) and exactly in the oracle; at the largest position here
-(16383 * theta_0) the fp32 angle is off by at most ~1e-3 rad, well inside the
-tolerance.
+<= 5e-2).  The rotation fused into the projection's epilogue takes cos/sin of
+angles formed and reduced in fp64 (exact to fp32 rounding at every position);
+the separate rotation pass (with the query-key norm) builds its angles in fp32
+as the page prescribes, off by at most ~1e-3 rad at 16383 * theta_0, well
+inside the tolerance.  The oracle rotates exactly.
 """
 import numpy as np
 import pytest
@@ -171,3 +172,77 @@ def test_rope_rejects_odd_head_dim(ssa):
     with pytest.raises(ssa.SsaError) as e:
         ssa.ssa_forward(x.cuda(), {k: v.cuda() for k, v in p.items()}, 4, 16, rope=True)
     assert e.value.status == 1
+
+
+ROPE_STEP_SHAPES = [
+    # name, B, C, H, W, G, h, dtype        epilogue path of the fused rotation
+    ("d32", 1, 64, 8, 8, 8, 2, "f32"),       # the tiny shape: 16-column chunks
+    ("d48", 2, 96, 9, 16, 8, 2, "f32"),      # d = dp = 48: 16-column chunks, whole pairs
+    ("d64", 2, 128, 12, 20, 8, 2, "f32"),    # 32-column chunks: shuffle-transposed stores
+    ("d272", 1, 272, 6, 22, 16, 1, "f32"),   # d = 272 -> 288: a chunk of pure zero padding
+    ("d512", 1, 512, 12, 25, 32, 1, "f32"),  # one head of 512 across four slices
+    ("c768-d64-bf16", 2, 768, 8, 16, 32, 12, "bf16"),  # C > 512: staged 8-feature halves, TMA stores
+]
+
+
+@pytest.mark.parametrize("case", ROPE_STEP_SHAPES, ids=[c[0] for c in ROPE_STEP_SHAPES])
+def test_qkv_project_rope_step_against_oracle(ssa, case):
+    """The rotation fused into the projection's epilogue: Q at sampled pixels
+    and K at every pixel against the oracle's rotated projections (exact
+    angles in fp64); V as without the rotation."""
+    name, B, C, H, W, G, h, dt = case
+    wl, x, p, _ = _inputs(B, C, H, W, G, h, dt, seed=C + H)
+    p = {k: v for k, v in p.items() if not k.startswith("_")}
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    _, _, a, s = ssa.ssa_gn_stats(xd, G, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, h)
+    q, k, vt = ssa.ssa_qkv_project_rope(xd, a, s, pk["w_qkv"], pk["b_qkv"], h)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    N, d = H * W, C // h
+    qi = np.arange(0, N, 7)
+    r = oracle.forward(x, p, G, h, qidx=qi, want=("q", "k", "v"), rope=True)
+    qg = q[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, N, C)[:, qi]
+    kg = k[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, N, C)
+    vg = vt[:, :, :d, :N].double().cpu().numpy().transpose(0, 3, 1, 2).reshape(B, N, C)
+    for got, ref in ((qg, r["q"]), (kg, r["k"]), (vg, r["v"])):
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 3e-3
+        np.testing.assert_allclose(got, ref, rtol=4e-3, atol=4e-3)
+    dp = ssa.layout(B, C, H, W, h)["dp"]
+    if d < dp:
+        assert torch.count_nonzero(q[..., d:dp]) == 0 and torch.count_nonzero(k[..., d:dp]) == 0
+
+
+def test_qkv_project_rope_rejects_plain_order_shapes(ssa):
+    """Head dims that are not a multiple of 16 keep Q/K rows in plain order
+    (the rotation then runs as its own pass): the fused entry point says so."""
+    wl, x, p, _ = _inputs(1, 80, 8, 8, 8, 2, "f32", seed=9)   # d = 40
+    p = {k: v for k, v in p.items() if not k.startswith("_")}
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    _, _, a, s = ssa.ssa_gn_stats(xd, 8, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, 2)
+    with pytest.raises(ssa.SsaError) as e:
+        ssa.ssa_qkv_project_rope(xd, a, s, pk["w_qkv"], pk["b_qkv"], 2)
+    assert e.value.status == 4
+
+
+@pytest.mark.parametrize("name", ["unet-lowres", "vae16384"])
+def test_named_workload_rope_positions(ssa, name):
+    """Fused rotation at every token position of the named grids whose head
+    dims take it (the largest angle is 16383 rad at theta_0 = 1 on
+    128 x 128): K against the oracle."""
+    wl = wls.WORKLOADS[name]
+    x, p, _ = wls.make_inputs(wl)
+    xd = x.cuda()
+    pd = {k: v.cuda() for k, v in p.items()}
+    _, _, a, s = ssa.ssa_gn_stats(xd, wl.num_groups, pd["norm_weight"], pd["norm_bias"])
+    pk = ssa.ssa_pack_weights(pd, wl.num_heads)
+    q, k, vt = ssa.ssa_qkv_project_rope(xd, a, s, pk["w_qkv"], pk["b_qkv"], wl.num_heads)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    B, C, N, h = wl.B, wl.C, wl.N, wl.num_heads
+    d = C // h
+    r = oracle.forward(x, p, wl.num_groups, h, qidx=np.array([N - 1]), want=("k",), rope=True)
+    kg = k[..., :d].double().cpu().numpy().transpose(0, 2, 1, 3).reshape(B, N, C)
+    assert np.linalg.norm(kg - r["k"]) / np.linalg.norm(r["k"]) < 3e-3
+    np.testing.assert_allclose(kg, r["k"], rtol=4e-3, atol=8e-3)
