@@ -17,6 +17,9 @@ import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libssa_gb300.so")
+# The same library built with bf16 tensor-core operands (for comparing the two
+# operand types; fp16 is the default).
+LIB_PATHS = {"f16": LIB_PATH, "bf16": os.path.join(PKG, "libssa_gb300_bf16.so")}
 
 SSA_F32, SSA_BF16 = 0, 1
 STATUS = {0: "SSA_OK", 1: "SSA_ERR_CONSTRAINT", 2: "SSA_ERR_DTYPE", 3: "SSA_ERR_ALIGNMENT",
@@ -48,6 +51,22 @@ class SsaError(RuntimeError):
 
 
 _lib = None
+_libs = {}
+_operand = "f16"
+
+
+def set_operand_type(operand: str):
+    """Selects the library the calls below go through: 'f16' (default) or
+    'bf16' tensor-core operands.  Process-wide."""
+    global _operand, _lib
+    if operand not in LIB_PATHS:
+        raise ValueError(operand)
+    _operand = operand
+    _lib = _libs.get(operand)
+
+
+def operand_type() -> str:
+    return _operand
 
 
 def load_library():
@@ -55,9 +74,10 @@ def load_library():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is not built; run `python -m diffusion_net_spatial_gb300.build`")
-    lib = ctypes.CDLL(LIB_PATH)
+    path = LIB_PATHS[_operand]
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m diffusion_net_spatial_gb300.build`")
+    lib = ctypes.CDLL(path)
     vp, i32, sz, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
     sig = {
         "ssa_workspace_size": ([i32] * 7, sz),
@@ -95,6 +115,7 @@ def load_library():
         fn.argtypes = args
         fn.restype = res
     _lib = lib
+    _libs[_operand] = lib
     return lib
 
 

@@ -536,7 +536,7 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
           for (int i = 0; i < 32; i += 2) {
             float t0, t1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ex2_f16x2(pack_half2(t0, t1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = exp2_pair_op(t0, t1);
           }
       } else {
         // the row sum in four paired accumulators
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
             const float e0 = ex2_approx(t0);
             const float e1 = ex2_approx(t1);
             acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
-            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_half2(e0, e1);
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_op2(e0, e1);
           }
         float s0, s1, s2, s3;
         f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
@@ -623,21 +623,20 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
         const int e0 = oc * args.d_o + cc * 16;
         if (vec && e0 + 16 <= args.d) {
           uint4 w0, w1;
-          w0.x = pack_half2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
-          w0.y = pack_half2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
-          w0.z = pack_half2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
-          w0.w = pack_half2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
-          w1.x = pack_half2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
-          w1.y = pack_half2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
-          w1.z = pack_half2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
-          w1.w = pack_half2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
+          w0.x = pack_op2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
+          w0.y = pack_op2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
+          w0.z = pack_op2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
+          w0.w = pack_op2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
+          w1.x = pack_op2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
+          w1.y = pack_op2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
+          w1.z = pack_op2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
+          w1.w = pack_op2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
           reinterpret_cast<uint4 *>(orow + e0)[0] = w0;
           reinterpret_cast<uint4 *>(orow + e0)[1] = w1;
         } else {
           for (int i = 0; i < 16; ++i) {
             if (e0 + i < args.d) {
-              const __half hv = __float2half_rn(__uint_as_float(t[i]) * inv);
-              orow[e0 + i] = *reinterpret_cast<const uint16_t *>(&hv);
+              orow[e0 + i] = op_bits(__uint_as_float(t[i]) * inv);
             }
           }
         }
@@ -810,7 +809,7 @@ __device__ __forceinline__ void store_o32(uint16_t *o_w, int ldc, int rows_valid
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
+      for (int m = 0; m < 4; ++m) a[k][m] = pack_op2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       // (lane j of the group, piece k) -> (lane k, piece j)
@@ -837,8 +836,7 @@ __device__ __forceinline__ void store_o32(uint16_t *o_w, int ldc, int rows_valid
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (e0 + i < d) {
-        const __half hv = __float2half_rn(v[i]);
-        orow[e0 + i] = *reinterpret_cast<const uint16_t *>(&hv);
+        orow[e0 + i] = op_bits(v[i]);
       }
   }
 }
@@ -1114,7 +1112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
               const float e0 = ex2_approx(t0);
               const float e1 = ex2_approx(t1);
               acc2[(i >> 3) & 3] = f2_add(acc2[(i >> 3) & 3], f2_pack(e0, e1));
-              pk[c * 16 + (i >> 1)] = pack_half2(e0, e1);
+              pk[c * 16 + (i >> 1)] = pack_op2(e0, e1);
             }
           float s0, s1, s2, s3;
           f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);

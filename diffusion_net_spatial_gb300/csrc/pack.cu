@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ssa {
 namespace {
@@ -26,10 +27,7 @@ __device__ __forceinline__ float ld_param(const void *p, long long i) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
 
-__device__ __forceinline__ uint16_t to_half_bits(float v) {
-  const __half h = __float2half_rn(v);
-  return *reinterpret_cast<const uint16_t *>(&h);
-}
+__device__ __forceinline__ uint16_t to_half_bits(float v) { return op_bits(v); }
 
 template <int DT>
 __global__ void pack_kernel(int C, int h, int d, int dp, int ldc, int inter, const void *wq, const void *bq,

@@ -383,11 +383,20 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
+// 16-bit tensor-core operand type of the library: fp16, or bf16 when it is
+// built with SSA_OPERAND_BF16 (a second library, for comparing the two).
+#ifdef SSA_OPERAND_BF16
+constexpr uint32_t kOpFormat = 1;  // kind::f16 A/B format code: bf16
+#else
+constexpr uint32_t kOpFormat = 0;  // fp16
+#endif
+
+// Instruction descriptor, kind::f16: A and B of the operand type (both
+// K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
   return (1u << 4)              // D format: f32
-         | (0u << 7)            // A format: f16
-         | (0u << 10)           // B format: f16
+         | (kOpFormat << 7)     // A format
+         | (kOpFormat << 10)    // B format
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16
 }
@@ -399,22 +408,48 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
 }
 
 // ------------------------------------------------------------------ misc ----
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+// Two fp32 values rounded (to nearest even) to the operand type, packed
+// with `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_op2(float lo, float hi) {
   uint32_t r;
+#ifdef SSA_OPERAND_BF16
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+#else
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+#endif
   return r;
+}
+// One value of the operand type (bits) from fp32, and back.
+__device__ __forceinline__ uint16_t op_bits(float v) { return (uint16_t)(pack_op2(v, 0.f) & 0xFFFFu); }
+__device__ __forceinline__ float op_to_float(uint16_t b) {
+#ifdef SSA_OPERAND_BF16
+  return __uint_as_float(((uint32_t)b) << 16);
+#else
+  float f;
+  asm("{\n\t.reg .b16 h;\n\tmov.b16 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "h"(b));
+  return f;
+#endif
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x for two fp16 values at once (low and high halves of a packed pair):
-// one MUFU operation for two results, the output already packed for the MMA.
-__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+// (2^t0, 2^t1) in the operand type, packed.  fp16 operands: the exponents
+// rounded to fp16 and raised together (one MUFU operation for two results);
+// bf16 keeps too few exponent bits for that, so there the fp32 powers are
+// rounded once.
+__device__ __forceinline__ uint32_t exp2_pair_op(float t0, float t1) {
+#ifdef SSA_OPERAND_BF16
+  float y0, y1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(t0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y1) : "f"(t1));
+  return pack_op2(y0, y1);
+#else
   uint32_t y;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(pack_op2(t0, t1)));
   return y;
+#endif
 }
 // Packed fp32 pairs (one 64-bit register): Blackwell's paired FMA/ADD issue
 // two fp32 operations per instruction.

@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           z[i] = fmaf(slot[j * 8 + i], xv, slot[32 + j * 8 + i]);
         }
-        st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_half2(z[0], z[1]),
-                     pack_half2(z[2], z[3]), pack_half2(z[4], z[5]), pack_half2(z[6], z[7]));
+        st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_op2(z[0], z[1]),
+                     pack_op2(z[2], z[3]), pack_op2(z[4], z[5]), pack_op2(z[6], z[7]));
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -342,24 +342,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 8; ++j) rope_pair(v[2 * j], v[2 * j + 1], t, th[i0 + j]);
           }
           uint4 wx, wy;
-          wx.x = pack_half2(v[0], v[2]); wx.y = pack_half2(v[4], v[6]);
-          wx.z = pack_half2(v[8], v[10]); wx.w = pack_half2(v[12], v[14]);
-          wy.x = pack_half2(v[1], v[3]); wy.y = pack_half2(v[5], v[7]);
-          wy.z = pack_half2(v[9], v[11]); wy.w = pack_half2(v[13], v[15]);
+          wx.x = pack_op2(v[0], v[2]); wx.y = pack_op2(v[4], v[6]);
+          wx.z = pack_op2(v[8], v[10]); wx.w = pack_op2(v[12], v[14]);
+          wy.x = pack_op2(v[1], v[3]); wy.y = pack_op2(v[5], v[7]);
+          wy.z = pack_op2(v[9], v[11]); wy.w = pack_op2(v[13], v[15]);
           reinterpret_cast<uint4 *>(chunk)[row] = wx;
           reinterpret_cast<uint4 *>(chunk + 2048)[row] = wy;
         } else if (sec < 2) {
           uint4 w0, w1;
-          w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
-          w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
-          w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
-          w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
+          w0.x = pack_op2(v[0], v[1]); w0.y = pack_op2(v[2], v[3]);
+          w0.z = pack_op2(v[4], v[5]); w0.w = pack_op2(v[6], v[7]);
+          w1.x = pack_op2(v[8], v[9]); w1.y = pack_op2(v[10], v[11]);
+          w1.z = pack_op2(v[12], v[13]); w1.w = pack_op2(v[14], v[15]);
           reinterpret_cast<uint4 *>(chunk + row * 32)[0] = w0;
           reinterpret_cast<uint4 *>(chunk + row * 32)[1] = w1;
         } else {
-          __half *vt_rows = reinterpret_cast<__half *>(chunk);
+          uint16_t *vt_rows = reinterpret_cast<uint16_t *>(chunk);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) vt_rows[i * BM + row] = __float2half_rn(v[i]);
+          for (int i = 0; i < 16; ++i) vt_rows[i * BM + row] = op_bits(v[i]);
         }
       }
       fence_proxy_async_smem();
@@ -484,9 +484,9 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
   const int pix = p0 + row;
   if (sec == 2) {
     // this warp's V^T staging: [CW features][32 pixels], 64-byte rows
-    __half *st = reinterpret_cast<__half *>(vst);
+    uint16_t *st = reinterpret_cast<uint16_t *>(vst);
 #pragma unroll
-    for (int k = 0; k < CW; ++k) st[k * 32 + lane] = __float2half_rn(v[k]);
+    for (int k = 0; k < CW; ++k) st[k * 32 + lane] = op_bits(v[k]);
     return;
   }
   const long long bh = (long long)b * args.h + hd;
@@ -510,8 +510,8 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int j = 8 * k + 2 * m;
-          a[k][m] = pack_half2(v[2 * j], v[2 * j + 2]);
-          a[2 + k][m] = pack_half2(v[2 * j + 1], v[2 * j + 3]);
+          a[k][m] = pack_op2(v[2 * j], v[2 * j + 2]);
+          a[2 + k][m] = pack_op2(v[2 * j + 1], v[2 * j + 3]);
         }
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -541,8 +541,8 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
     uint32_t xw[CW / 4], yw[CW / 4];
 #pragma unroll
     for (int m = 0; m < CW / 4; ++m) {
-      xw[m] = pack_half2(v[4 * m], v[4 * m + 2]);
-      yw[m] = pack_half2(v[4 * m + 1], v[4 * m + 3]);
+      xw[m] = pack_op2(v[4 * m], v[4 * m + 2]);
+      yw[m] = pack_op2(v[4 * m + 1], v[4 * m + 3]);
     }
     store_run<CW / 2>(dst + i0, xw, npair);
     store_run<CW / 2>(dst + hd2 + i0, yw, npair);
@@ -555,7 +555,7 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) a[k][m] = pack_half2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
+      for (int m = 0; m < 4; ++m) a[k][m] = pack_op2(v[8 * k + 2 * m], v[8 * k + 2 * m + 1]);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const uint32_t s0 = (j4 & 1) ? a[0][m] : a[1][m];
@@ -580,10 +580,10 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
     if (pix >= args.N) return;
     uint16_t *dst = qk + (long long)pix * args.ldq + r0;
     uint4 w0, w1;
-    w0.x = pack_half2(v[0], v[1]); w0.y = pack_half2(v[2], v[3]);
-    w0.z = pack_half2(v[4], v[5]); w0.w = pack_half2(v[6], v[7]);
-    w1.x = pack_half2(v[8], v[9]); w1.y = pack_half2(v[10], v[11]);
-    w1.z = pack_half2(v[12], v[13]); w1.w = pack_half2(v[14], v[15]);
+    w0.x = pack_op2(v[0], v[1]); w0.y = pack_op2(v[2], v[3]);
+    w0.z = pack_op2(v[4], v[5]); w0.w = pack_op2(v[6], v[7]);
+    w1.x = pack_op2(v[8], v[9]); w1.y = pack_op2(v[10], v[11]);
+    w1.z = pack_op2(v[12], v[13]); w1.w = pack_op2(v[14], v[15]);
     reinterpret_cast<uint4 *>(dst)[0] = w0;
     reinterpret_cast<uint4 *>(dst)[1] = w1;
   }
@@ -787,7 +787,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
           x1 = __uint_as_float(((uint32_t)reinterpret_cast<const unsigned short *>(xs)[(ch + 1) * BM + px]) << 16);
         }
         // channels past C are zero (their scale and shift are zero)
-        w[i] = pack_half2(fmaf(slot[2 * i], x0, slot[32 + 2 * i]), fmaf(slot[2 * i + 1], x1, slot[32 + 2 * i + 1]));
+        w[i] = pack_op2(fmaf(slot[2 * i], x0, slot[32 + 2 * i]), fmaf(slot[2 * i + 1], x1, slot[32 + 2 * i + 1]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xfree[s]);  // the x block has been read

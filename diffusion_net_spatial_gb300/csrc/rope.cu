@@ -21,6 +21,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ssa {
 namespace {
@@ -42,11 +43,11 @@ __global__ void rope_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int
     uint16_t *bufs[2] = {q, k};
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      __half *p = reinterpret_cast<__half *>(bufs[u]) + row * ldq;
-      const float a = __half2float(p[i]);
-      const float b = __half2float(p[hd + i]);
-      p[i] = __float2half_rn(a * cs - b * sn);
-      p[hd + i] = __float2half_rn(b * cs + a * sn);
+      uint16_t *p = bufs[u] + row * ldq;
+      const float a = op_to_float(p[i]);
+      const float b = op_to_float(p[hd + i]);
+      p[i] = op_bits(a * cs - b * sn);
+      p[hd + i] = op_bits(b * cs + a * sn);
     }
   }
 }
@@ -70,18 +71,18 @@ __global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, long long rows, int N, 
     const int which = wr >= rows ? 1 : 0;
     const long long row = wr - which * rows;
     const int head = (int)((row / N) % h);
-    __half *p = reinterpret_cast<__half *>(which ? k : q) + row * ldq;
+    uint16_t *p = (which ? k : q) + row * ldq;
     const void *g = which ? kg : qg;
     float ss = 0.f;
     for (int e = lane; e < d; e += 32) {
-      const float v = __half2float(p[e]);
+      const float v = op_to_float(p[e]);
       ss = fmaf(v, v, ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
     const float scale = sd / fmaxf(sqrtf(ss), 1e-12f);
     for (int e = lane; e < d; e += 32)
-      p[e] = __float2half_rn(__half2float(p[e]) * scale * ld_x<DT>(g, (long long)head * d + e));
+      p[e] = op_bits(op_to_float(p[e]) * scale * ld_x<DT>(g, (long long)head * d + e));
   }
 }
 

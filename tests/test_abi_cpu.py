@@ -109,3 +109,15 @@ def test_attention_scratch_size_and_split_policy(lib):
     assert lib.ssa_set_attention_split(7) == 1
     for p in (ssa.SPLIT_ALWAYS, ssa.SPLIT_NEVER, ssa.SPLIT_AUTO):
         assert lib.ssa_set_attention_split(p) == 0
+
+
+def test_bf16_operand_library_exports_the_same_boundary(lib):
+    """The same sources built with bf16 tensor-core operands (for the operand
+    comparison) load and export every declared function too."""
+    path = ssa.LIB_PATHS["bf16"]
+    if not os.path.exists(path):
+        from diffusion_net_spatial_gb300 import build
+        build.build()
+    other = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(other, name), name
