@@ -414,8 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 //   warp 1       MMA warp (warp-uniform loop, elected lane issues)
 //   warps 2..9   converters (x block -> A columns in tensor memory), then
 //                epilogues (bias, the optional rotary embedding, fp16; Q/K
-//                rows stored directly, V^T staged in shared memory and
-//                written by TMA)
+//                rows and V^T rows stored directly)
 constexpr int RNST = 6;                  // ring slots of 32 KB
 constexpr int RSLOT = 32768;
 constexpr int RTHREADS = 352;
@@ -439,8 +438,7 @@ struct ResArgs {
 };
 // barriers: full[RNST], empty[RNST], xfree[RNST], a_ready, acc_full[2], acc_empty[2], drain
 constexpr int RNBARS = 3 * RNST + 6;
-constexpr uint32_t RES_VST_OFF = RNST * RSLOT;               // V^T staging: 4 KB per epilogue warp
-constexpr uint32_t RES_SLOT_OFF = RES_VST_OFF + 32768;       // converters' GN scale/shift staging
+constexpr uint32_t RES_SLOT_OFF = RNST * RSLOT;              // converters' GN scale/shift staging
 constexpr uint32_t RES_BARS_OFF = RES_SLOT_OFF + NCONV * 256;
 constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
 
@@ -451,13 +449,13 @@ constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
 //        features (two pieces per row; rows >= d of the packed head are the
 //        zero padding [d, dp));
 //   Q/K, plain order: the chunk's features as one piece per row;
-//   V:   into the warp's V^T staging area [CW features][32 pixels] at vst.
+//   V:   rows of V^T (feature-major), one 64-byte warp store per feature.
 // Q/K rows go straight to global memory; with CW = 32 a 4 x 4 shuffle
 // transpose inside each group of 4 lanes makes lanes 4g..4g+3 write the four
 // 16-byte pieces of one row per store instruction.
 template <int CW>
 __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t taddr, int F0, int b, int p0, int q4,
-                                              int lane, uint8_t *vst, const float2 *th) {
+                                              int lane, const float2 *th) {
   uint32_t r[CW];
   if constexpr (CW == 32) tmem_ld32(taddr, r);
   else tmem_ld16(taddr, r);
@@ -483,10 +481,15 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
   const int row = q4 * 32 + lane;
   const int pix = p0 + row;
   if (sec == 2) {
-    // this warp's V^T staging: [CW features][32 pixels], 64-byte rows
-    uint16_t *st = reinterpret_cast<uint16_t *>(vst);
+    // V^T row e holds feature e for every pixel: each store instruction of the
+    // warp writes 32 consecutive pixels (64 contiguous bytes) of one row.
+    // (Staging the rows in shared memory for TMA stores measured 2 us slower
+    // on both large workloads.)
+    if (pix < args.N) {
+      uint16_t *dst = args.vt + (((long long)b * args.h + hd) * args.dp + r0) * args.ldn + pix;
 #pragma unroll
-    for (int k = 0; k < CW; ++k) st[k * 32 + lane] = op_bits(v[k]);
+      for (int k = 0; k < CW; ++k) dst[(long long)k * args.ldn] = op_bits(v[k]);
+    }
     return;
   }
   const long long bh = (long long)b * args.h + hd;
@@ -592,7 +595,7 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
 template <int DT>
 __global__ void __launch_bounds__(RTHREADS, 1)
     qkv_resident_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                        const __grid_constant__ CUtensorMap vmap, const ResArgs args) {
+                        const ResArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
   // The layout needs a 1024-byte aligned base (128B-swizzled operands) and
@@ -645,7 +648,6 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&xmap);
     tma_prefetch_desc(&wmap);
-    tma_prefetch_desc(&vmap);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -800,12 +802,6 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       if (lane == 0) mbar_arrive(a_ready);
     }
     // ------------------------------------------------------------ epilogues
-    // Each warp stages its own V^T pieces ([CW features][32 pixels] per chunk,
-    // 4 KB per warp and slice) and writes them with its own TMA stores, so the
-    // eight warps never wait for one another; before refilling its staging a
-    // warp waits until its previous stores have read it.
-    uint8_t *vst = sm + RES_VST_OFF + cw * 4096;
-    bool stores_pending = false;
     // Rotation thetas in the converters' (now idle) scale/shift slots.  Every
     // epilogue warp takes both barriers, whatever its state.
     float2 *th = reinterpret_cast<float2 *>(sm + RES_SLOT_OFF);
@@ -814,52 +810,21 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       rope_thetas(th, args.d, cw * 32 + lane, NCONV * 32);
       named_bar_sync(1, NCONV * 32);
     }
-    const int hdp = args.h * args.dp;
     const int nch = args.BN / args.cw;
     for (int i = 0; i < nsl && ok; ++i) {
       const int buf = i & 1;
       if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
       const int fs = (sl0 + (i + rot) % nsl) * args.BN;
-      const bool has_v = fs + args.BN > 2 * hdp;
-      if (has_v && stores_pending) {
-        if (lane == 0) tma_store_wait_read();
-        __syncwarp();
-      }
       const uint32_t acc = lane_base + (uint32_t)(buf * 128);
-      int nv = 0;  // V chunks staged by this warp in this slice
       for (int c = hc; c < nch; c += 2) {
-        const int F0 = fs + c * args.cw;
-        uint8_t *vs = vst + nv * args.cw * 64;
-        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), F0, b, p0, q4, lane, vs, th);
-        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), F0, b, p0, q4, lane, vs, th);
-        if (F0 >= 2 * hdp) ++nv;
-      }
-      if (nv > 0) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          int k = 0;
-          for (int c = hc; c < nch; c += 2) {
-            const int F0 = fs + c * args.cw;
-            if (F0 < 2 * hdp) continue;
-            for (int u = 0; u < args.cw / 16; ++u) {
-              const int F = F0 + 16 * u;
-              tma_store_3d(&vmap, vst + (k * args.cw + 16 * u) * 64, p0 + q4 * 32, F % args.dp,
-                           b * args.h + (F / args.dp) % args.h);
-            }
-            ++k;
-          }
-          tma_store_commit();
-        }
-        stores_pending = true;
+        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), fs + c * 32, b, p0, q4, lane, th);
+        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), fs + c * 16, b, p0, q4, lane, th);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    if (stores_pending && lane == 0) tma_store_wait_all();
-    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -949,16 +914,7 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
       break;
     }
   if (resident_ok(dm) && BNr > 0 && BM * BK * es <= RSLOT) {
-    CUtensorMap wmap_r, vmap_r;
-    {
-      // V^T pieces of one epilogue warp: [16 features][32 pixels]
-      const uint64_t vdims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, (uint64_t)dm.B * dm.h};
-      const uint64_t vstrides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
-      const uint32_t vbox[3] = {32, 16, 1};
-      if (encode_tiled(&vmap_r, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, vdims, vstrides, vbox,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-        return 1;
-    }
+    CUtensorMap wmap_r;
     const int w3d = (dm.C % BK == 0) ? 1 : 0;
     if (w3d) {
       // W viewed as [64-channel chunk][feature][64 channels]: one box = two
@@ -999,10 +955,10 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
     const dim3 grid(ng, (dm.N + BM - 1) / BM, dm.B);
     if (dtype == 0) {
       cudaFuncSetAttribute(qkv_resident_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, vmap_r, r);
+      (void)launch_k(qkv_resident_kernel<0>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
     } else {
       cudaFuncSetAttribute(qkv_resident_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, vmap_r, r);
+      (void)launch_k(qkv_resident_kernel<1>, dim3(grid), dim3(RTHREADS), smem, st, xmap, wmap_r, r);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
   }
