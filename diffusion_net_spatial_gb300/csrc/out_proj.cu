@@ -440,17 +440,31 @@ __global__ void __launch_bounds__(ORTHREADS, 1)
     const int q4 = warp & 3;
     const int half = ew >> 2;
     const int row = q4 * 32 + lane;
+    // This warp's biases for every piece, fetched before any wait (lane l
+    // holds channel c0 + l of each 32-channel block; C <= 512 here, so at
+    // most 4 pieces x 2 blocks).
+    float bias_r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = (u >> 1) * 128 + half * 64 + (u & 1) * 32 + lane;
+      bias_r[u] = c < args.C ? __ldg(args.bias + c) : 0.f;
+    }
     bool ok = mbar_wait_warp(acc_full, 0, ab);
     for (int k = 0; k < args.npieces && ok; ++k) {
       const int bf = k & 1;
       if (!mbar_wait_warp(&xfull[bf], (uint32_t)((k >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
       uint8_t *xs = sm + bf * piece_bytes;
-      for (int c32 = 0; c32 < 64; c32 += 32) {
+#pragma unroll
+      for (int h32 = 0; h32 < 2; ++h32) {
+        const int c32 = h32 * 32;
         const int cl0 = half * 64 + c32;   // channel within the piece
         const int c0 = k * 128 + cl0;      // output channel
         if (c0 >= args.C) break;
-        const float bl = c0 + lane < args.C ? __ldg(args.bias + c0 + lane) : 0.f;
+        float bl = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          if (kk == k) bl = bias_r[2 * kk + h32];
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, r);
         tmem_wait_ld();

@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 //   warps 2..9   converters (x block -> A columns in tensor memory), then
 //                epilogues (bias, the optional rotary embedding, fp16; Q/K
 //                rows and V^T rows stored directly)
-constexpr int RNST = 6;                  // ring slots of 32 KB
+constexpr int RNST = 5;                  // ring slots of 32 KB (6 or 7 measured no faster: shared memory past the 164 KB carveout costs L1)
 constexpr int RSLOT = 32768;
 constexpr int RTHREADS = 352;
 constexpr uint32_t RA_COL = 256;         // A operand: tensor-memory columns 256 .. 256 + C/2
@@ -453,27 +453,18 @@ constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
 // Q/K rows go straight to global memory; with CW = 32 a 4 x 4 shuffle
 // transpose inside each group of 4 lanes makes lanes 4g..4g+3 write the four
 // 16-byte pieces of one row per store instruction.
+// `bl`: lane l holds the bias of the chunk's column l (fetched by the caller
+// before its wait for the accumulator), handed to every lane by shuffles.
 template <int CW>
 __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t taddr, int F0, int b, int p0, int q4,
-                                              int lane, const float2 *th) {
+                                              int lane, const float2 *th, float bl) {
   uint32_t r[CW];
   if constexpr (CW == 32) tmem_ld32(taddr, r);
   else tmem_ld16(taddr, r);
-  // The chunk's biases, the same for every lane (broadcast vector loads).
-  float bv[CW];
-  const float4 *bq = reinterpret_cast<const float4 *>(args.bias + F0);
-#pragma unroll
-  for (int k = 0; k < CW / 4; ++k) {
-    const float4 t4 = __ldg(bq + k);
-    bv[4 * k] = t4.x;
-    bv[4 * k + 1] = t4.y;
-    bv[4 * k + 2] = t4.z;
-    bv[4 * k + 3] = t4.w;
-  }
   tmem_wait_ld();
   float v[CW];
 #pragma unroll
-  for (int k = 0; k < CW; ++k) v[k] = __uint_as_float(r[k]) + bv[k];
+  for (int k = 0; k < CW; ++k) v[k] = __uint_as_float(r[k]) + __shfl_sync(0xFFFFFFFFu, bl, k);
   const int hdp = args.h * args.dp;
   const int sec = F0 / hdp;
   const int hd = (F0 / args.dp) % args.h;
@@ -813,13 +804,24 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const int nch = args.BN / args.cw;
     for (int i = 0; i < nsl && ok; ++i) {
       const int buf = i & 1;
+      const int fs = (sl0 + (i + rot) % nsl) * args.BN;
+      // this warp's chunk biases (lane l: column l of chunk u), fetched before
+      // the wait so their latency hides behind it
+      float bl[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = hc + 2 * u;
+        bl[u] = (c < nch && lane < args.cw) ? __ldg(args.bias + fs + c * args.cw + lane) : 0.f;
+      }
       if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
-      const int fs = (sl0 + (i + rot) % nsl) * args.BN;
       const uint32_t acc = lane_base + (uint32_t)(buf * 128);
-      for (int c = hc; c < nch; c += 2) {
-        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), fs + c * 32, b, p0, q4, lane, th);
-        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), fs + c * 16, b, p0, q4, lane, th);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = hc + 2 * u;
+        if (c >= nch) break;
+        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), fs + c * 32, b, p0, q4, lane, th, bl[u]);
+        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), fs + c * 16, b, p0, q4, lane, th, bl[u]);
       }
       tc_fence_before();
       __syncwarp();
