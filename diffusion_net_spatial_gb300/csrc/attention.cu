@@ -655,6 +655,333 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
 
 
 // ---------------------------------------------------------------------------
+// Quad mode (padded head dim <= 64, the block without a mask or table): four
+// query tiles in flight per SM.  The single mode's 128-key tiles need 256
+// tensor-memory columns per query tile (S, P, O), so an SM holds two query
+// tiles: each tile's chain of softmax steps sets the pace, and on unet-l1 the
+// 512 query tiles leave a partial second wave on 304 CTA slots.  Here a key
+// tile is 64 keys and P is written over the scores it came from, so a query
+// tile needs 128 columns; a CTA holds QT query tiles (of the same sample and
+// head) that share one K/V ring:
+//   tensor memory (128 per query tile t): S_j at 128t + 0..63 (fp32), then
+//                P_j at 128t + 0..31 (fp16 pairs), O at 128t + 64..64+dp
+//   shared memory: QT Q tiles [128 x 64] and QNST ring slots, each the K box
+//                [64 keys x 64 dims] and the V^T box [dp x 64 keys]
+//   warp 0   TMA producer;  warp 1 MMA: for each query tile t in turn,
+//            once its softmax has written P_tj, O_t += P_tj V_j (P from
+//            tensor memory), and once that has completed (same columns)
+//            S_t(j+1) = Q_t K_(j+1)^T
+//   warps 2.. softmax, four per query tile, one query row per thread: the
+//            tile's 64 scores in one tensor-memory round trip (the longest
+//            stall of the loop), the row maximum, then P per 32 keys stored
+//            over scores already read
+// With QT = 2 and two CTAs per SM the 152 SMs hold 608 query tiles at once
+// (one wave for unet-l1), sixteen softmax warps per SM, and each K/V tile is
+// loaded once for two query tiles.
+constexpr int QK = 64;                           // keys per tile
+constexpr int QNST = 3;                          // ring slots
+constexpr int QSLOT = 16384;                     // K (8 KB) + V^T (<= 8 KB)
+constexpr uint32_t Q_TM_O = 64;                  // O inside a query tile's 128 columns
+template <int QT> struct QuadCfg {
+  static constexpr int THREADS = 64 + 128 * QT;
+  static constexpr int NBARS = 2 * QNST + 3 * QT + 2;  // full, empty, q_full, s_full[QT], p_full[QT], o_done[QT], drain
+  static constexpr uint32_t OFF_RING = 16384u * QT;
+  static constexpr uint32_t OFF_BARS = OFF_RING + QNST * QSLOT;
+  static constexpr uint32_t SMEM = OFF_BARS + NBARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 128u * QT;
+};
+
+template <int QT>
+__global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
+    attention_quad_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
+  using Cfg = QuadCfg<QT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw;
+  // 128B-swizzled operands need a 1024-byte aligned base; the layout leaves
+  // no room to realign, so refuse to run otherwise.
+  if ((smem_u32(sm) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicOr(args.err, (uint32_t)DEV_MISALIGNED);
+    return;
+  }
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Cfg::OFF_BARS);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + QNST;
+  uint64_t *q_full = bars + 2 * QNST;
+  uint64_t *s_full = q_full + 1;   // [QT]
+  uint64_t *p_full = s_full + QT;  // [QT]
+  uint64_t *o_done = p_full + QT;  // [QT]
+  uint64_t *drain = o_done + QT;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NBARS);
+  volatile uint32_t *abort_flag = tmem_slot + 1;
+  uint8_t *ring = sm + Cfg::OFF_RING;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * BQ * QT;
+  const int bh = blockIdx.y;
+  const int n = (args.N + QK - 1) / QK;  // key tiles
+  const uint32_t vbytes = (uint32_t)args.dp * 128u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < QNST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // inputs of the previous kernel visible from here on
+  const Abort ab{abort_flag, args.err, args.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 16384u * QT);
+      for (int t = 0; t < QT; ++t) tma_load_3d(sm + t * 16384, &qmap, q_full, 0, q0 + t * BQ, bh);
+      int it = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % QNST;
+        if (args.stall && (uint32_t)it >= args.stall) break;  // test hook: consumers' waits expire
+        if (j >= QNST && !mbar_wait(&empty[s], (uint32_t)(((j / QNST) - 1) & 1), ab)) break;
+        mbar_arrive_expect_tx(&full[s], 8192u + vbytes);
+        tma_load_3d(ring + s * QSLOT, &kmap, &full[s], 0, j * QK, bh);
+        tma_load_3d(ring + s * QSLOT + 8192, &vmap, &full[s], j * QK, 0, bh);
+        ++it;
+      }
+      // Never leave with a copy in flight.
+      mbar_wait_drain(q_full, 0, drain_limit(ab));
+      for (int i = (it > QNST ? it - QNST : 0); i < it; ++i)
+        mbar_wait_drain(&full[i % QNST], (uint32_t)((i / QNST) & 1), drain_limit(ab));
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA warp
+    const uint32_t idesc_s = idesc_f16(BQ, QK);
+    const uint32_t idesc_o = idesc_f16(BQ, (uint32_t)args.dp);
+    const uint64_t qd = sdesc_k128(smem_u32(sm));
+    const uint64_t rd = sdesc_k128(smem_u32(ring));
+    const int ksteps = args.dp / 16;
+    // Each query tile runs its own chain P_tj -> O_t += P_tj V_j -> S_t(j+1);
+    // the tiles are served in turn, so one tile's softmax overlaps the other's
+    // MMAs.  S_t(j+1) overwrites the columns P_tj V_j reads: it is issued only
+    // once that P V has completed.
+    auto issue_s = [&](int t, int j) {
+      const uint64_t kd = rd + (uint64_t)(((j % QNST) * QSLOT) >> 4);
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          if (kk < ksteps)
+            mma_f16_ss(tmem + (uint32_t)(t * 128), qd + (uint64_t)(t * 1024 + kk * 2), kd + (uint64_t)(kk * 2),
+                       idesc_s, kk ? 1u : 0u);
+        mma_commit(&s_full[t]);
+      }
+      __syncwarp();
+    };
+    bool ok = mbar_wait_warp(q_full, 0, ab) && mbar_wait_warp(&full[0], 0, ab), issued = false;
+    if (ok) {
+      for (int t = 0; t < QT; ++t) issue_s(t, 0);
+      issued = true;
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      const int s = j % QNST;
+      const uint64_t vd = rd + (uint64_t)((s * QSLOT + 8192) >> 4);
+      bool next_full = false;
+      for (int t = 0; t < QT; ++t) {
+        if (!mbar_wait_warp(&p_full[t], (uint32_t)(j & 1), ab)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // 16 keys (8 columns of P) per step
+            mma_f16_ts(tmem + (uint32_t)(t * 128) + Q_TM_O, tmem + (uint32_t)(t * 128 + kk * 8),
+                       vd + (uint64_t)(kk * 2), idesc_o, (j | kk) ? 1u : 0u);
+          mma_commit(&o_done[t]);
+        }
+        __syncwarp();
+        if (j + 1 < n) {
+          if (!next_full) {
+            if (!mbar_wait_warp(&full[(j + 1) % QNST], (uint32_t)(((j + 1) / QNST) & 1), ab)) { ok = false; break; }
+            next_full = true;
+          }
+          if (!mbar_wait_warp(&o_done[t], (uint32_t)(j & 1), ab)) { ok = false; break; }
+          issue_s(t, j + 1);
+        }
+      }
+      if (ok) {  // slot s is free once this tile's MMAs complete
+        if (elect_one()) mma_commit(&empty[s]);
+        __syncwarp();
+      }
+    }
+    if (issued) {  // every issued MMA completes before tensor memory is freed
+      if (elect_one()) mma_commit(drain);
+      __syncwarp();
+      mbar_wait_drain(drain, 0, drain_limit(ab));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qt = (warp - 2) >> 2;  // this warp's query tile
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int query = q0 + qt * BQ + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(qt * 128);
+    const float sl2 = args.sl2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait_warp(&s_full[qt], (uint32_t)(j & 1), ab)) { ok = false; break; }
+      tc_fence_after();
+      const int kvalid = min(QK, args.N - j * QK);
+      // The tile's 64 scores in one round trip (both loads, one wait): the
+      // wait for tensor memory is the longest stall of this loop.
+      uint32_t r[2][32];
+      tmem_ld32(lane_base, r[0]);
+      tmem_ld32(lane_base + 32u, r[1]);
+      tmem_wait_ld();
+      if (kvalid < QK) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
+      }
+      float pm[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = t >> 1, o = (t & 1) * 16;
+        float m = __uint_as_float(r[c][o]);
+#pragma unroll
+        for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
+        pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
+      }
+      const float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
+      const float m_new = fmaxf(m_used, mx * sl2);
+      // Lazy rescale, decided per warp (as in the single mode).
+      const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
+      const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (rescale && m_new > m_used) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+      }
+      if (rescale) {
+        // O is idle: the P V of the previous tile completed before S_j was issued.
+        for (int cc = 0; cc < args.dp / 16; ++cc) {
+          uint32_t t[16];
+          tmem_ld16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+          tmem_st16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
+        }
+      }
+      // P per 32 keys into columns 16c.. (scores already in registers).
+      const uint64_t c2 = f2_pack(sl2, sl2);
+      const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+        if (args.ones) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+            pk[i >> 1] = exp2_pair_op(t0, t1);
+          }
+        } else {
+          uint64_t acc2[2] = {0ull, 0ull};
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+            const float e0 = ex2_approx(t0);
+            const float e1 = ex2_approx(t1);
+            acc2[(i >> 1) & 1] = f2_add(acc2[(i >> 1) & 1], f2_pack(e0, e1));
+            pk[i >> 1] = pack_op2(e0, e1);
+          }
+          float s0, s1;
+          f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+          sum += s0 + s1;
+        }
+        tmem_st16(lane_base + (uint32_t)(16 * c), pk);
+      }
+      l = l * alpha + sum;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[qt]);
+    }
+    // ------------------------------------------------------------ epilogue
+    const bool eok = ok && mbar_wait_warp(&o_done[qt], (uint32_t)((n - 1) & 1), ab);
+    if (eok) {
+      __syncwarp();
+      tc_fence_after();
+      if (args.ones) {
+        l = __uint_as_float(tmem_ld1(lane_base + Q_TM_O + (uint32_t)args.d));  // O column d = sum of P
+        tmem_wait_ld();
+      }
+      const float inv = 1.0f / l;
+      const int b = bh / args.h, hd = bh % args.h;
+      const bool vec = (args.d % 8) == 0;
+      uint16_t *orow = args.o + ((long long)b * args.N + query) * args.ldc + (long long)hd * args.d;
+      for (int cc = 0; cc < args.dp / 16; ++cc) {
+        uint32_t t[16];
+        tmem_ld16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
+        tmem_wait_ld();
+        if (query >= args.N) continue;
+        const int e0 = cc * 16;
+        if (vec && e0 + 16 <= args.d) {
+          uint4 w0, w1;
+          w0.x = pack_op2(__uint_as_float(t[0]) * inv, __uint_as_float(t[1]) * inv);
+          w0.y = pack_op2(__uint_as_float(t[2]) * inv, __uint_as_float(t[3]) * inv);
+          w0.z = pack_op2(__uint_as_float(t[4]) * inv, __uint_as_float(t[5]) * inv);
+          w0.w = pack_op2(__uint_as_float(t[6]) * inv, __uint_as_float(t[7]) * inv);
+          w1.x = pack_op2(__uint_as_float(t[8]) * inv, __uint_as_float(t[9]) * inv);
+          w1.y = pack_op2(__uint_as_float(t[10]) * inv, __uint_as_float(t[11]) * inv);
+          w1.z = pack_op2(__uint_as_float(t[12]) * inv, __uint_as_float(t[13]) * inv);
+          w1.w = pack_op2(__uint_as_float(t[14]) * inv, __uint_as_float(t[15]) * inv);
+          reinterpret_cast<uint4 *>(orow + e0)[0] = w0;
+          reinterpret_cast<uint4 *>(orow + e0)[1] = w1;
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (e0 + i < args.d) orow[e0 + i] = op_bits(__uint_as_float(t[i]) * inv);
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Pair mode (padded head dim 512).  O for 128 queries fills all 512 tensor-
 // memory columns, so one CTA cannot hold O and the scores at once.  A cluster
 // of two CTAs on two SMs shares one query tile at a time and splits the work
@@ -1493,6 +1820,53 @@ int launch_attention_pair(const Dims &dm, AttnArgs a, const uint16_t *q, const u
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 
+int launch_attention_quad(const Dims &dm, AttnArgs a, const uint16_t *q, const uint16_t *k, const uint16_t *vt,
+                          uint16_t *o, const KParams &kp, cudaStream_t st) {
+  a.sl2 = 1.4426950408889634f / sqrtf((float)dm.d);
+  a.o = o;
+  a.err = kp.err;
+  a.timeout_ns = kp.timeout_ns;
+  a.stall = stall_for(kp, STALL_ATTENTION);
+  a.ones = dm.dp > dm.d ? 1 : 0;  // V^T row d holds ones (the weight pack sets that bias)
+  CUtensorMap qmap, kmap, vmap;
+  const uint64_t BH = (uint64_t)dm.B * dm.h;
+  {
+    const uint64_t dims[3] = {(uint64_t)dm.ldq, (uint64_t)dm.N, BH};
+    const uint64_t strides[2] = {(uint64_t)dm.ldq * 2, (uint64_t)dm.N * dm.ldq * 2};
+    const uint32_t qbox[3] = {64, BQ, 1};
+    const uint32_t kbox[3] = {64, QK, 1};
+    if (encode_tiled(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, strides, qbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+    if (encode_tiled(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, strides, kbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.dp, BH};
+    const uint64_t strides[2] = {(uint64_t)dm.ldn * 2, (uint64_t)dm.dp * dm.ldn * 2};
+    const uint32_t box[3] = {QK, (uint32_t)dm.dp, 1};
+    if (encode_tiled(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vt, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+  }
+  // Two query tiles per CTA whenever there are two; one otherwise.
+  const int nqt = (dm.N + BQ - 1) / BQ;
+  if (nqt >= 2) {
+    auto kern = attention_quad_kernel<2>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QuadCfg<2>::SMEM);
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    (void)launch_k(kern, dim3((nqt + 1) / 2, (unsigned)BH, 1), dim3(QuadCfg<2>::THREADS), QuadCfg<2>::SMEM, st, qmap,
+                   kmap, vmap, a);
+  } else {
+    auto kern = attention_quad_kernel<1>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QuadCfg<1>::SMEM);
+    (void)launch_k(kern, dim3((unsigned)nqt, (unsigned)BH, 1), dim3(QuadCfg<1>::THREADS), QuadCfg<1>::SMEM, st, qmap,
+                   kmap, vmap, a);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
 }  // namespace
 
 size_t attention_scratch_bytes(const Dims &dm) {
@@ -1517,6 +1891,7 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
     a.N = dm.N; a.h = dm.h; a.d = dm.d; a.ldc = dm.ldc;
     return launch_attention_pair(dm, a, q, k, vt, scratch, st);
   }
+  if (dm.dp <= 64 && !causal && rel == nullptr) return launch_attention_quad(dm, a, q, k, vt, o, kp, st);
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

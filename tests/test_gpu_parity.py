@@ -297,7 +297,8 @@ ABORT_CASES = [
     # name, B, C, H, W, G, h, dtype, kernel whose producer stalls
     ("qkv-resident", 2, 320, 32, 32, 32, 8, "f32", 1),       # resident QKV (C <= 512), both producer warps
     ("qkv-general", 2, 768, 8, 16, 32, 12, "bf16", 1),       # QKV for C > 512
-    ("attention-single", 2, 320, 32, 32, 32, 8, "f32", 2),   # single mode (two CTAs per SM), d = 40
+    ("attention-quad", 2, 320, 32, 32, 32, 8, "f32", 2),     # quad mode (head dim <= 64), d = 40
+    ("attention-single", 1, 256, 32, 32, 32, 2, "f32", 2),   # single mode (two CTAs per SM), d = 128
     ("attention-double", 1, 320, 16, 16, 16, 1, "f32", 2),   # double mode (two O halves), d = 320
     ("out-proj-resident", 2, 320, 64, 64, 32, 8, "f32", 4),  # resident out-projection (C <= 512, >= 64 tiles)
     ("out-proj-small", 2, 320, 32, 32, 32, 8, "f32", 4),     # out-projection, one tile per CTA (16 tiles)
