@@ -12,7 +12,7 @@
 //
 // qk_norm_kernel: query-key RMS normalisation (vit-pytorch
 // simple_vit_with_qk_norm.py, RMSNorm class): each head's Q and K rows become
-// x / max(||x||_2, 1e-12) * sqrt(d) * gamma[head][:], one warp per row, fp32
+// x / max(||x||_2, 1e-12) * sqrt(d) * gamma[head][:], eight lanes per row, fp32
 // sum of squares, rounded back to fp16 once.
 //
 // rel_table_pack_kernel: the learned table [(2H-1)(2W-1)][heads] in x's dtype
@@ -26,29 +26,31 @@
 namespace ssa {
 namespace {
 
-__global__ void rope_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int ldq, int d) {
+// One thread per (row, pair i), consecutive threads on consecutive pairs of a
+// row; the angle bases theta_i = 10000^(-2i/d) come from a table each block
+// builds once in shared memory, and the index arithmetic is 32-bit.
+__global__ void rope_kernel(uint16_t *q, uint16_t *k, int total, int N, int ldq, int d) {
+  __shared__ float theta[256];
   pdl_trigger();
-  pdl_wait();
   const int hd = d / 2;
-  const long long total = rows * hd;
   const float l2base = -2.0f * 13.287712379549449f / (float)d;  // -2 log2(10000) / d
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long row = idx / hd;
-    const int i = (int)(idx - row * hd);
-    const int t = (int)(row % N);
-    const float theta = exp2f(l2base * (float)i);
+  for (int i = threadIdx.x; i < hd; i += blockDim.x) theta[i] = exp2f(l2base * (float)i);
+  __syncthreads();
+  pdl_wait();
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+    const int row = idx / hd;
+    const int i = idx - row * hd;
+    const float t = (float)(row % N);
     float sn, cs;
-    sincosf((float)t * theta, &sn, &cs);
-    uint16_t *bufs[2] = {q, k};
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      uint16_t *p = bufs[u] + row * ldq;
-      const float a = op_to_float(p[i]);
-      const float b = op_to_float(p[hd + i]);
-      p[i] = op_bits(a * cs - b * sn);
-      p[hd + i] = op_bits(b * cs + a * sn);
-    }
+    sincosf(t * theta[i], &sn, &cs);
+    uint16_t *pq = q + (long long)row * ldq;
+    uint16_t *pk = k + (long long)row * ldq;
+    const float qa = op_to_float(pq[i]), qb = op_to_float(pq[hd + i]);
+    const float ka = op_to_float(pk[i]), kb = op_to_float(pk[hd + i]);
+    pq[i] = op_bits(qa * cs - qb * sn);
+    pq[hd + i] = op_bits(qb * cs + qa * sn);
+    pk[i] = op_bits(ka * cs - kb * sn);
+    pk[hd + i] = op_bits(kb * cs + ka * sn);
   }
 }
 
@@ -59,30 +61,63 @@ __device__ __forceinline__ float ld_x(const void *p, long long i) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
 
+// Eight lanes per row (Q rows, then K rows), so a warp touches four rows'
+// contiguous bytes: lane j takes the 16-byte pieces j, j + 8, ... of the row
+// when the head dim is a multiple of 8 (rows start 128-byte aligned), else
+// elements j, j + 8, ...; the sum of squares is combined by shuffles inside
+// the group of eight and the row is scaled on a second read (from L1).
 template <int DT>
-__global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, long long rows, int N, int h, int ldq, int d,
-                               const void *qg, const void *kg) {
+__global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, int rows, int N, int h, int ldq, int d, const void *qg,
+                               const void *kg) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const float sd = sqrtf((float)d);
-  for (long long wr = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); wr < 2 * rows; wr += nwarps) {
-    const int which = wr >= rows ? 1 : 0;
-    const long long row = wr - which * rows;
-    const int head = (int)((row / N) % h);
-    uint16_t *p = (which ? k : q) + row * ldq;
-    const void *g = which ? kg : qg;
-    float ss = 0.f;
-    for (int e = lane; e < d; e += 32) {
+  const int wr = (blockIdx.x * blockDim.x + threadIdx.x) >> 3;  // uniform within a group of eight lanes
+  const int j = threadIdx.x & 7;
+  if (wr >= 2 * rows) return;
+  const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+  const int which = wr >= rows ? 1 : 0;
+  const int row = wr - which * rows;
+  const int head = (row / N) % h;
+  uint16_t *p = (which ? k : q) + (long long)row * ldq;
+  const void *g = which ? kg : qg;
+  const long long g0 = (long long)head * d;
+  const bool vec = (d % 8) == 0;
+  float ss = 0.f;
+  if (vec) {
+    for (int e = 8 * j; e < d; e += 64) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(p + e);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float a = op_to_float((uint16_t)(w[m] & 0xFFFFu)), b = op_to_float((uint16_t)(w[m] >> 16));
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+  } else {
+    for (int e = j; e < d; e += 8) {
       const float v = op_to_float(p[e]);
       ss = fmaf(v, v, ss);
     }
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    const float scale = sd / fmaxf(sqrtf(ss), 1e-12f);
-    for (int e = lane; e < d; e += 32)
-      p[e] = op_bits(op_to_float(p[e]) * scale * ld_x<DT>(g, (long long)head * d + e));
+  for (int o = 4; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
+  const float scale = sqrtf((float)d) / fmaxf(sqrtf(ss), 1e-12f);
+  if (vec) {
+    for (int e = 8 * j; e < d; e += 64) {
+      uint4 u = *reinterpret_cast<const uint4 *>(p + e);
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float a = op_to_float((uint16_t)(w[m] & 0xFFFFu)) * scale * ld_x<DT>(g, g0 + e + 2 * m);
+        const float b = op_to_float((uint16_t)(w[m] >> 16)) * scale * ld_x<DT>(g, g0 + e + 2 * m + 1);
+        w[m] = (uint32_t)op_bits(a) | ((uint32_t)op_bits(b) << 16);
+      }
+      u.x = w[0]; u.y = w[1]; u.z = w[2]; u.w = w[3];
+      *reinterpret_cast<uint4 *>(p + e) = u;
+    }
+  } else {
+    for (int e = j; e < d; e += 8) p[e] = op_bits(op_to_float(p[e]) * scale * ld_x<DT>(g, g0 + e));
   }
 }
 
@@ -116,20 +151,23 @@ int grid_for(long long work) {
 }  // namespace
 
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st) {
-  const long long rows = (long long)dm.B * dm.h * dm.N;
-  (void)launch_k(rope_kernel, dim3(grid_for(rows * (dm.d / 2))), dim3(256), 0, st, q, k, rows, dm.N, dm.ldq, dm.d);
+  const long long total = (long long)dm.B * dm.h * dm.N * (dm.d / 2);
+  if (dm.d / 2 > 256 || total >= (1LL << 31)) return cudaErrorInvalidValue;
+  (void)launch_k(rope_kernel, dim3(grid_for(total)), dim3(256), 0, st, q, k, (int)total, dm.N, dm.ldq, dm.d);
   return cudaGetLastError();
 }
 
 cudaError_t launch_qk_norm(const Dims &dm, int dtype, uint16_t *q, uint16_t *k, const void *q_gamma,
                            const void *k_gamma, cudaStream_t st) {
   const long long rows = (long long)dm.B * dm.h * dm.N;
-  long long blocks = (2 * rows + 7) / 8;  // 8 warps (rows) per block
-  if (blocks > 8192) blocks = 8192;
+  if (16 * rows >= (1LL << 31)) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((16 * rows + 127) / 128));  // eight lanes per row, Q and K
   if (dtype == 0)
-    (void)launch_k(qk_norm_kernel<0>, dim3((int)blocks), dim3(256), 0, st, q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
+    (void)launch_k(qk_norm_kernel<0>, grid, dim3(128), 0, st, q, k, (int)rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma,
+                   k_gamma);
   else
-    (void)launch_k(qk_norm_kernel<1>, dim3((int)blocks), dim3(256), 0, st, q, k, rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma, k_gamma);
+    (void)launch_k(qk_norm_kernel<1>, grid, dim3(128), 0, st, q, k, (int)rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma,
+                   k_gamma);
   return cudaGetLastError();
 }
 
