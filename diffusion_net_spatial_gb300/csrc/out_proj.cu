@@ -510,7 +510,19 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
                               (reinterpret_cast<uintptr_t>(out) & 15u) == 0
                           ? 1
                           : 0;
-  const int BN = pick_bn(dm.C, tma_epi ? 128 : 256);
+  int BN = pick_bn(dm.C, tma_epi ? 128 : 256);
+  int max_smem = 232448, dev = 0, nsm = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  }
+  // Few pixel tiles (at most half as many as SMs): two CTAs per pixel tile,
+  // each computing half of the output channels, keep more SMs busy than one
+  // CTA per tile with all channels (unet-l1: 64 tiles, block 130 -> 127 us).
+  const int mtiles = dm.B * ((dm.N + BM - 1) / BM);
+  const bool half_split = tma_epi && 2 * mtiles <= nsm && dm.C % 32 == 0 && dm.C / 2 <= 256 &&
+                          (int)smem_total(dm.C / 2, 1, es) <= max_smem;
+  if (half_split) BN = dm.C / 2;
   CUtensorMap omap, wmap, xmap, outmap;
   {
     const uint64_t dims[3] = {(uint64_t)dm.C, (uint64_t)dm.N, (uint64_t)dm.B};
@@ -540,14 +552,10 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
     outmap = omap;
   }
   const int nkb = (dm.C + BK - 1) / BK;
-  int max_smem = 232448, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   const int c16 = (dm.C + 15) / 16 * 16;
   // The resident form pays off when there are enough pixel tiles to fill the
   // GPU with one CTA each.
-  const int mtiles = dm.B * ((dm.N + BM - 1) / BM);
-  if (tma_epi && c16 <= 512 && mtiles >= 64 && (int)ores_smem(nkb) <= max_smem &&
+  if (!half_split && tma_epi && c16 <= 512 && mtiles >= 64 && (int)ores_smem(nkb) <= max_smem &&
       2u * 128u * 128u * (uint32_t)es <= ores_bars_off(nkb)) {
     const int nch = (c16 + 255) / 256;
     const int BNc = ((c16 / nch + 15) / 16) * 16;

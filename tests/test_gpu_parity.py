@@ -300,7 +300,8 @@ ABORT_CASES = [
     ("attention-quad", 2, 320, 32, 32, 32, 8, "f32", 2),     # quad mode (head dim <= 64), d = 40
     ("attention-single", 1, 256, 32, 32, 32, 2, "f32", 2),   # single mode (two CTAs per SM), d = 128
     ("attention-double", 1, 320, 16, 16, 16, 1, "f32", 2),   # double mode (two O halves), d = 320
-    ("out-proj-resident", 2, 320, 64, 64, 32, 8, "f32", 4),  # resident out-projection (C <= 512, >= 64 tiles)
+    ("out-proj-resident", 5, 256, 48, 48, 32, 4, "f32", 4),  # resident out-projection (C <= 512, 90 tiles)
+    ("out-proj-halves", 2, 320, 64, 64, 32, 8, "f32", 4),    # 64 tiles: two CTAs per tile, half the channels each
     ("out-proj-small", 2, 320, 32, 32, 32, 8, "f32", 4),     # out-projection, one tile per CTA (16 tiles)
     ("out-proj-general", 2, 768, 8, 16, 32, 12, "bf16", 4),  # out-projection for C > 512
 ]
