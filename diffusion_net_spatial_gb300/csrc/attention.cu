@@ -691,7 +691,86 @@ template <int QT> struct QuadCfg {
   static constexpr uint32_t TMEM_COLS = 128u * QT;
 };
 
-template <int QT>
+// Relative-position table of the quad mode (W a multiple of 32): a warp's 32
+// queries lie in one grid row and each 32-key chunk in one grid row, so the
+// chunk's 32 x 32 bias block is a Toeplitz slice of one table row, read as
+// p[-i] from one per-lane pointer p (one L1 load per score, coalesced).  The
+// warp's grid position is fixed and the key tile's is advanced by additions,
+// so no division runs per key tile.  Scores become base-2 logits
+// s * log2(e)/sqrt(d) + table, two per paired FMA.
+struct QuadTable {
+  const float *row0;  // this head's packed table
+  int row_len, gw, gh, rq_off;  // 2W - 1, W, H, (query grid row) + H - 1
+  int cq_off;               // (first query's grid column) + W - 1
+  int rk, ck;               // grid row and column of the current key tile's first key
+  bool valid;               // the warp's queries exist
+};
+
+__device__ __forceinline__ void quad_table_init(QuadTable &t, const AttnArgs &args, int head, int qw) {
+  t.row_len = 2 * args.gw - 1;
+  t.gw = args.gw;
+  t.gh = args.gh;
+  t.valid = qw < args.N;
+  const int rq = t.valid ? qw / args.gw : 0;
+  t.rq_off = rq + args.gh - 1;
+  t.cq_off = (t.valid ? qw - rq * args.gw : 0) + args.gw - 1;
+  t.row0 = args.rel + (long long)head * args.tabn;
+  t.rk = 0;
+  t.ck = 0;
+}
+
+// Pointer p of the chunk whose first key is at grid (rk, ck).
+__device__ __forceinline__ const float *quad_table_ptr(const QuadTable &t, int rk, int ck, int lane) {
+  return t.row0 + (t.rq_off - rk) * t.row_len + (t.cq_off - ck) + lane;
+}
+
+// Logits of the key tile at (t.rk, t.ck), 64 keys; keys past N are already
+// -inf and stay so.  Then t advances to the next key tile, whose table rows
+// are prefetched into L1.
+__device__ __forceinline__ void quad_table_apply(QuadTable &t, uint32_t (&r)[2][32], float sl2, int kvalid,
+                                                 int lane) {
+  const uint64_t c2 = f2_pack(sl2, sl2);
+  int rk = t.rk, ck = t.ck;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (t.valid && 32 * c < kvalid) {
+      const float *p = quad_table_ptr(t, rk, ck, lane);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2,
+                         f2_pack(__ldg(p - i), __ldg(p - i - 1))),
+                  a0, a1);
+        r[c][i] = __float_as_uint(a0);
+        r[c][i + 1] = __float_as_uint(a1);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[c][i] = __float_as_uint(__uint_as_float(r[c][i]) * sl2);
+    }
+    ck += 32;
+    if (ck == t.gw) {
+      ck = 0;
+      ++rk;
+    }
+  }
+  t.rk = rk;
+  t.ck = ck;
+  if (t.valid) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const bool wrap = ck + 32 * c >= t.gw;
+      if (rk + (wrap ? 1 : 0) >= t.gh) continue;  // past the last key row
+      const float *p = quad_table_ptr(t, rk + (wrap ? 1 : 0), wrap ? ck + 32 * c - t.gw : ck + 32 * c, lane);
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p - 31));
+    }
+  }
+}
+
+// VAR 1: the relative-position table over a width that is a multiple of 32
+// (the Toeplitz path of apply_variants); its scores become base-2 logits.
+template <int QT, int VAR>
 __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
     attention_quad_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const AttnArgs args) {
@@ -847,6 +926,8 @@ __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
     const float sl2 = args.sl2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    QuadTable tab;
+    if constexpr (VAR != 0) quad_table_init(tab, args, bh % args.h, query - lane);
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(&s_full[qt], (uint32_t)(j & 1), ab)) { ok = false; break; }
       tc_fence_after();
@@ -864,6 +945,7 @@ __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
+      if constexpr (VAR != 0) quad_table_apply(tab, r, sl2, kvalid, lane);
       float pm[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -874,7 +956,7 @@ __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
         pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
       }
       const float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
-      const float m_new = fmaxf(m_used, mx * sl2);
+      const float m_new = fmaxf(m_used, VAR != 0 ? mx : mx * sl2);
       // Lazy rescale, decided per warp (as in the single mode).
       const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
       const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
@@ -897,7 +979,8 @@ __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
         }
       }
       // P per 32 keys into columns 16c.. (scores already in registers).
-      const uint64_t c2 = f2_pack(sl2, sl2);
+      const float cs = VAR != 0 ? 1.f : sl2;  // logits already scaled
+      const uint64_t c2 = f2_pack(cs, cs);
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
       float sum = 0.f;
 #pragma unroll
@@ -1850,19 +1933,23 @@ int launch_attention_quad(const Dims &dm, AttnArgs a, const uint16_t *q, const u
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return 1;
   }
-  // Two query tiles per CTA whenever there are two; one otherwise.
+  // Two query tiles per CTA whenever there are two; one otherwise.  The
+  // table instances read the table through L1: shared memory only as large
+  // as two CTAs need (the plain ones take the whole carveout).
   const int nqt = (dm.N + BQ - 1) / BQ;
+  auto run = [&](auto kern, int qt, uint32_t smem, int threads, int carveout) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (carveout >= 0) cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+    (void)launch_k(kern, dim3((unsigned)((nqt + qt - 1) / qt), (unsigned)BH, 1), dim3(threads), smem, st, qmap, kmap,
+                   vmap, a);
+  };
+  const bool table = a.rel != nullptr;
   if (nqt >= 2) {
-    auto kern = attention_quad_kernel<2>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QuadCfg<2>::SMEM);
-    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    (void)launch_k(kern, dim3((nqt + 1) / 2, (unsigned)BH, 1), dim3(QuadCfg<2>::THREADS), QuadCfg<2>::SMEM, st, qmap,
-                   kmap, vmap, a);
+    if (table) run(attention_quad_kernel<2, 1>, 2, QuadCfg<2>::SMEM, QuadCfg<2>::THREADS, 72);
+    else run(attention_quad_kernel<2, 0>, 2, QuadCfg<2>::SMEM, QuadCfg<2>::THREADS, 100);
   } else {
-    auto kern = attention_quad_kernel<1>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QuadCfg<1>::SMEM);
-    (void)launch_k(kern, dim3((unsigned)nqt, (unsigned)BH, 1), dim3(QuadCfg<1>::THREADS), QuadCfg<1>::SMEM, st, qmap,
-                   kmap, vmap, a);
+    if (table) run(attention_quad_kernel<1, 1>, 1, QuadCfg<1>::SMEM, QuadCfg<1>::THREADS, -1);
+    else run(attention_quad_kernel<1, 0>, 1, QuadCfg<1>::SMEM, QuadCfg<1>::THREADS, -1);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
@@ -1891,7 +1978,8 @@ int launch_attention(const Dims &dm, const uint16_t *q, const uint16_t *k, const
     a.N = dm.N; a.h = dm.h; a.d = dm.d; a.ldc = dm.ldc;
     return launch_attention_pair(dm, a, q, k, vt, scratch, st);
   }
-  if (dm.dp <= 64 && !causal && rel == nullptr) return launch_attention_quad(dm, a, q, k, vt, o, kp, st);
+  if (dm.dp <= 64 && !causal && (rel == nullptr || dm.W % 32 == 0))
+    return launch_attention_quad(dm, a, q, k, vt, o, kp, st);
   int max_smem = MAX_SMEM_FALLBACK, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

@@ -64,6 +64,8 @@ SHAPES = [
     ("d320", 1, 320, 10, 10, 16, 1, "f32"),   # double (two 160-wide O halves)
     ("d512", 1, 512, 12, 25, 32, 1, "f32"),   # pair, N = 300 (three 128-key tiles, ragged)
     ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
+    ("d64-w32", 1, 128, 6, 32, 8, 2, "f32"),  # quad, W % 32 == 0: the table path; N = 192 (ragged tile)
+    ("d40-w64", 1, 80, 3, 64, 8, 2, "f32"),   # quad with the ones column, W = 64
 ]
 VARIANTS = ["no_bias", "causal", "rope", "rel", "causal_rel", "qk_norm", "qk_norm_rope", "all"]
 
@@ -110,11 +112,13 @@ def test_planned_variants_match_one_shot(ssa):
         plan.close()
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "no-mask"])
 @pytest.mark.parametrize("name", ["unet-l1", "vae16384"])
-def test_named_workload_causal_rel(ssa, name):
-    """The two largest workloads with the causal mask and a relative-position
-    table over their full grids (64 x 64 with 8 heads; 128 x 128 with one
-    head of 512); the oracle evaluates a seeded sample of 128 query pixels."""
+def test_named_workload_causal_rel(ssa, name, causal):
+    """The two largest workloads with a relative-position table over their
+    full grids (64 x 64 with 8 heads; 128 x 128 with one head of 512), with
+    and without the causal mask; the oracle evaluates a seeded sample of 128
+    query pixels."""
     wl = wls.WORKLOADS[name]
     x, p, _ = wls.make_inputs(wl)
     g = torch.Generator().manual_seed(17)  # (the named workloads carry no QK-norm weights)
@@ -122,9 +126,9 @@ def test_named_workload_causal_rel(ssa, name):
     qidx = np.sort(torch.randperm(wl.N, generator=g)[:128].numpy())
     xd = x.cuda()
     pd = {k: v.cuda() for k, v in p.items()}
-    out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads, causal=True, rel_table=rel.cuda())
+    out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads, causal=causal, rel_table=rel.cuda())
     assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
-    _check(ssa, out, x, p, wl, qidx=qidx, causal=True, rel_table=rel.double().numpy())
+    _check(ssa, out, x, p, wl, qidx=qidx, causal=causal, rel_table=rel.double().numpy())
 
 
 def test_rope_step_against_oracle(ssa):
