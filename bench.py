@@ -405,6 +405,21 @@ def run_ours(args, rank, world, local):
         ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=dev)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    if args.forward_only:
+        # Profiling driver: only the planned forwards of this workload (W then
+        # K of them), so an ncu capture of one kernel sees few launches.
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup + args.steps):
+                plan.forward(xd, out=out, workspace=ws, stream=stream)
+        torch.cuda.synchronize(dev)
+        st = ssa.ssa_get_device_status(stream)
+        if rank == 0:
+            print(json.dumps({"forward_only": True, "workload": wl.name, "forwards": args.warmup + args.steps,
+                              "status": st}), flush=True)
+        plan.close()
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
+        return
     st = time_block(ssa, plan, xd, out, ws, flush, stream, max(3, args.warmup), 0)[0]
     K = args.steps
     barrier(world)
@@ -550,6 +565,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="skip the second workload's entry")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="run warmup + steps planned forwards and nothing else (a profiling driver; no timing line)")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     try:

@@ -12,6 +12,9 @@
 // global scratch and no second launch are needed.  The cluster's rank-0 CTA
 // writes mean, rstd = 1/sqrt(var + 1e-5) (biased variance) and the folded
 // affine a = rstd * weight, s = bias - mean * a for the group's channels.
+// x is read with an L2 evict-last hint: the projection reads the same x next,
+// and keeping it in L2 measured 1.8 us (unet-l1) and 3.1 us (vae16384) off
+// the block.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -44,6 +47,15 @@ __device__ __forceinline__ float load_scalar(const void *x, long long i) {
   if (DT == 0) return __ldg(reinterpret_cast<const float *>(x) + i);
   const unsigned short u = __ldg(reinterpret_cast<const unsigned short *>(x) + i);
   return __uint_as_float(((uint32_t)u) << 16);
+}
+
+// 16 bytes of x, kept in L2 (evict-last) for the projection that reads x next.
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
 }
 
 template <int DT>
@@ -104,12 +116,14 @@ __global__ void __launch_bounds__(kThreads, 2) gn_stats_kernel(const void *__res
   // batch; most slices need one or two batches).
   const uint4 *xv = reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(x) +
                                                     (base + a0) * (DT == 0 ? 4 : 2));
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   for (long long v = tid; v < nvec; v += (long long)UNROLL * kThreads) {
     uint4 r[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const long long idx = v + (long long)u * kThreads;
-      r[u] = idx < nvec ? __ldg(xv + idx) : make_uint4(0u, 0u, 0u, 0u);
+      r[u] = idx < nvec ? ld_keep(xv + idx, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
     // The batch's mean and M2, two-pass over its valid vectors (the
     // missing ones read as zeros and are left out of the count and of M2).
