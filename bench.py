@@ -407,15 +407,33 @@ def run_ours(args, rank, world, local):
 
     if args.forward_only:
         # Profiling driver: only the planned forwards of this workload (W then
-        # K of them), so an ncu capture of one kernel sees few launches.
+        # K of them), so an ncu capture of one kernel sees few launches;
+        # --variant selects one attention variant (seeded like the bench's).
+        fkw = {}
+        if args.variant != "none":
+            g = torch.Generator().manual_seed(wl.seed + 1234)
+            d = wl.C // wl.num_heads
+            if args.variant == "causal":
+                fkw = {"causal": True}
+            elif args.variant == "rope":
+                fkw = {"rope": True}
+            elif args.variant == "rel":
+                rel = (torch.rand((2 * wl.H - 1) * (2 * wl.W - 1), wl.num_heads, generator=g) * 2 - 1)
+                fkw = {"rel_table": rel.to(xd.dtype).to(dev)}
+            else:  # qk_norm
+                fkw = {"q_norm_weight": (0.5 + torch.rand(wl.num_heads, d, generator=g)).to(xd.dtype).to(dev),
+                       "k_norm_weight": (0.5 + torch.rand(wl.num_heads, d, generator=g)).to(xd.dtype).to(dev)}
         with torch.cuda.stream(stream):
+            # (the variants' table and scratch need more than the plain block)
+            fws = ws if not fkw else torch.empty(max(plan.workspace_size(wl.B, wl.H, wl.W) * 2, 1 << 20),
+                                                 dtype=torch.uint8, device=dev)
             for _ in range(args.warmup + args.steps):
-                plan.forward(xd, out=out, workspace=ws, stream=stream)
+                plan.forward(xd, out=out, workspace=fws, stream=stream, **fkw)
         torch.cuda.synchronize(dev)
         st = ssa.ssa_get_device_status(stream)
         if rank == 0:
-            print(json.dumps({"forward_only": True, "workload": wl.name, "forwards": args.warmup + args.steps,
-                              "status": st}), flush=True)
+            print(json.dumps({"forward_only": True, "workload": wl.name, "variant": args.variant,
+                              "forwards": args.warmup + args.steps, "status": st}), flush=True)
         plan.close()
         if st != 0:
             raise RuntimeError(f"device status {st}: {ssa.ssa_last_error_string()}")
@@ -567,6 +585,8 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the second workload's entry")
     ap.add_argument("--forward-only", action="store_true",
                     help="run warmup + steps planned forwards and nothing else (a profiling driver; no timing line)")
+    ap.add_argument("--variant", default="none", choices=["none", "causal", "rope", "rel", "qk_norm"],
+                    help="with --forward-only: the attention variant of the forwards")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     try:
