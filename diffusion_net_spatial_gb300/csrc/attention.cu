@@ -946,69 +946,117 @@ __global__ void __launch_bounds__(QuadCfg<QT>::THREADS, 2)
             if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
       }
       if constexpr (VAR != 0) quad_table_apply(tab, r, sl2, kvalid, lane);
-      float pm[4];
+      float alpha = 1.f, sum = 0.f;
+      bool done = false;
+#ifndef SSA_OPERAND_BF16
+      if (VAR == 0 && j > 0 && args.ones) {
+        // The exponents with the running maximum, as the fp16 pairs that
+        // ex2.approx.f16x2 takes (packed in place over consumed scores); their
+        // maximum by packed fp16 maxima decides the lazy rescale, so the fp32
+        // row maximum is only taken on the rare tiles that need one.
+        const uint64_t c2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-m_used, -m_used);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int c = t >> 1, o = (t & 1) * 16;
-        float m = __uint_as_float(r[c][o]);
-#pragma unroll
-        for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
-        pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
-      }
-      const float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
-      const float m_new = fmaxf(m_used, VAR != 0 ? mx : mx * sl2);
-      // Lazy rescale, decided per warp (as in the single mode).
-      const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
-      const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
-      float alpha = 1.f;
-      if (j == 0) {
-        m_used = m_new;
-      } else if (rescale && m_new > m_used) {
-        alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-      }
-      if (rescale) {
-        // O is idle: the P V of the previous tile completed before S_j was issued.
-        for (int cc = 0; cc < args.dp / 16; ++cc) {
-          uint32_t t[16];
-          tmem_ld16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-          tmem_st16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
-        }
-      }
-      // P per 32 keys into columns 16c.. (scores already in registers).
-      const float cs = VAR != 0 ? 1.f : sl2;  // logits already scaled
-      const uint64_t c2 = f2_pack(cs, cs);
-      const uint64_t nm2 = f2_pack(-m_used, -m_used);
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-        if (args.ones) {
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             float t0, t1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-            pk[i >> 1] = exp2_pair_op(t0, t1);
+            r[c][i >> 1] = pack_op2(t0, t1);
           }
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) h[k] = hmax2(r[k >> 3][2 * (k & 7)], r[k >> 3][2 * (k & 7) + 1]);
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) h[k] = hmax2(h[k], h[k + w]);
+        if (!__any_sync(0xFFFFFFFFu, h2_hmax(h[0]) > RESCALE_LOG2)) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[c][k] = ex2_h2(r[c][k]);
+            tmem_st16_lo(lane_base + (uint32_t)(16 * c), r[c]);
+          }
+          done = true;
         } else {
-          uint64_t acc2[2] = {0ull, 0ull};
+          // Rescale: the scores again from tensor memory (P has not been written).
+          tmem_ld32(lane_base, r[0]);
+          tmem_ld32(lane_base + 32u, r[1]);
+          tmem_wait_ld();
+          if (kvalid < QK) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float t0, t1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
-            const float e0 = ex2_approx(t0);
-            const float e1 = ex2_approx(t1);
-            acc2[(i >> 1) & 1] = f2_add(acc2[(i >> 1) & 1], f2_pack(e0, e1));
-            pk[i >> 1] = pack_op2(e0, e1);
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (32 * c + i >= kvalid) r[c][i] = __float_as_uint(-INFINITY);
           }
-          float s0, s1;
-          f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
-          sum += s0 + s1;
         }
-        tmem_st16(lane_base + (uint32_t)(16 * c), pk);
+      }
+#endif
+      if (!done) {
+        float pm[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = t >> 1, o = (t & 1) * 16;
+          float m = __uint_as_float(r[c][o]);
+#pragma unroll
+          for (int i = 1; i < 15; i += 2) m = max3f(m, __uint_as_float(r[c][o + i]), __uint_as_float(r[c][o + i + 1]));
+          pm[t] = fmaxf(m, __uint_as_float(r[c][o + 15]));
+        }
+        const float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
+        const float m_new = fmaxf(m_used, VAR != 0 ? mx : mx * sl2);
+        // Lazy rescale, decided per warp (as in the single mode).
+        const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
+        const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (rescale && m_new > m_used) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+        }
+        if (rescale) {
+          // O is idle: the P V of the previous tile completed before S_j was issued.
+          for (int cc = 0; cc < args.dp / 16; ++cc) {
+            uint32_t t[16];
+            tmem_ld16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st16(lane_base + Q_TM_O + (uint32_t)(cc * 16), t);
+          }
+        }
+        // P per 32 keys into columns 16c.. (scores already in registers).
+        const float cs = VAR != 0 ? 1.f : sl2;  // logits already scaled
+        const uint64_t c2 = f2_pack(cs, cs);
+        const uint64_t nm2 = f2_pack(-m_used, -m_used);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+          if (args.ones) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float t0, t1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+              pk[i >> 1] = exp2_pair_op(t0, t1);
+            }
+          } else {
+            uint64_t acc2[2] = {0ull, 0ull};
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float t0, t1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), c2, nm2), t0, t1);
+              const float e0 = ex2_approx(t0);
+              const float e1 = ex2_approx(t1);
+              acc2[(i >> 1) & 1] = f2_add(acc2[(i >> 1) & 1], f2_pack(e0, e1));
+              pk[i >> 1] = pack_op2(e0, e1);
+            }
+            float s0, s1;
+            f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+            sum += s0 + s1;
+          }
+          tmem_st16(lane_base + (uint32_t)(16 * c), pk);
+        }
       }
       l = l * alpha + sum;
       tmem_wait_st();
