@@ -523,6 +523,29 @@ int launch_out_proj(const Dims &dm, int dtype, const uint16_t *o, const uint16_t
   const bool half_split = tma_epi && 2 * mtiles <= nsm && dm.C % 32 == 0 && dm.C / 2 <= 256 &&
                           (int)smem_total(dm.C / 2, 1, es) <= max_smem;
   if (half_split) BN = dm.C / 2;
+  if (!half_split && tma_epi) {
+    // Channel tile by a simple cost model: each CTA streams its O tile
+    // (16 KB per 64-channel K step) and its Wo slice (BN x 128 bytes per
+    // step), so a wave of CTAs costs ~(16384 + 128 BN) per step, and the
+    // grid takes ceil(CTAs / (SMs x CTAs per SM)) waves.  E.g. unet-lowres
+    // (16 pixel tiles, C = 1280): 160 CTAs of 128 channels ran as 1 + 8/152
+    // waves; 128 CTAs of 160 channels take one.
+    // Tiles narrower than 64 channels are left out: their N < 64 MMAs run
+    // well below the tensor rate.
+    const int c16 = (dm.C + 15) / 16 * 16;
+    long long best = -1;
+    for (int bn = c16 < 64 ? c16 : 64; bn <= 256; bn += 16) {
+      const int sm_b = (int)smem_total(bn, 1, es);
+      if (c16 % bn != 0 || sm_b > max_smem) continue;
+      const long long per_sm = sm_b <= 113 * 1024 ? 2 : 1;
+      const long long ctas = (long long)(c16 / bn) * mtiles;
+      const long long cost = (ctas + nsm * per_sm - 1) / (nsm * per_sm) * (16384LL + 128LL * bn);
+      if (best < 0 || cost < best) {
+        best = cost;
+        BN = bn;
+      }
+    }
+  }
   CUtensorMap omap, wmap, xmap, outmap;
   {
     const uint64_t dims[3] = {(uint64_t)dm.C, (uint64_t)dm.N, (uint64_t)dm.B};
