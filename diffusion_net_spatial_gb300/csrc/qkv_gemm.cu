@@ -90,13 +90,13 @@ __device__ __forceinline__ void store_run(uint16_t *dst, const uint32_t (&w)[M /
   }
 }
 
-constexpr int XST = 2;      // x staging stages
+constexpr int XST = 4;      // x staging stages at most (args.xst: as many as shared memory allows, >= 2)
 constexpr int ST = 3;       // A/B operand stages
 constexpr int NCONV = 8;    // converter / epilogue warps
 constexpr int THREADS = (2 + NCONV) * 32;
 
 struct QkvArgs {
-  int C, N, h, dp, ldq, ldn, BN, nk, tmem_cols, xbytes;
+  int C, N, h, dp, ldq, ldn, BN, nk, tmem_cols, xbytes, xst;
   int d, inter;              // head dim; Q/K rows pair-interleaved (then d == dp, d % 16 == 0)
   int rope;                  // rotate Q and K in the epilogue (needs inter)
   uint32_t stall;            // test hook: the producer stops after this many loads (0: never)
@@ -115,10 +115,10 @@ struct Smem {
   uint32_t xs, as, bs, slot, bars;
 };
 
-__host__ __device__ inline Smem smem_layout(int xbytes, int BN) {
+__host__ __device__ inline Smem smem_layout(int xbytes, int BN, int xst) {
   Smem s;
   s.xs = 0;
-  s.as = s.xs + XST * xbytes;
+  s.as = s.xs + xst * xbytes;
   s.bs = s.as + ST * (BM * BK * 2);
   s.slot = s.bs + ST * (BN * BK * 2);
   s.bars = s.slot + NCONV * 256;
@@ -126,8 +126,8 @@ __host__ __device__ inline Smem smem_layout(int xbytes, int BN) {
 }
 // barriers: x_full[XST], x_empty[XST], b_full[ST], a_full[ST], ab_empty[ST], acc_full, drain, epi_done
 constexpr int NBARS = 2 * XST + 3 * ST + 3;
-__host__ __device__ inline uint32_t smem_total(int xbytes, int BN) {
-  return smem_layout(xbytes, BN).bars + NBARS * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
+__host__ __device__ inline uint32_t smem_total(int xbytes, int BN, int xst) {
+  return smem_layout(xbytes, BN, xst).bars + NBARS * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
 }
 
 template <int DT>
@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap vmap, const QkvArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Smem L = smem_layout(args.xbytes, args.BN);
+  const Smem L = smem_layout(args.xbytes, args.BN, args.xst);
+  const int xst = args.xst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
   uint64_t *x_full = bars;
   uint64_t *x_empty = bars + XST;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nk = args.nk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < XST; ++i) {
+    for (int i = 0; i < xst; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], NCONV);
     }
@@ -194,9 +195,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int nx = 0, nb = 0;
     if (lane == 0) {
       for (int kb = 0; kb < nk; ++kb) {
-        const int sx = kb % XST, s = kb % ST;
+        const int sx = kb % xst, s = kb % ST;
         if (args.stall && (uint32_t)(nx + nb) >= args.stall) break;  // test hook: consumers' waits expire
-        if (kb >= XST && !mbar_wait(&x_empty[sx], ((kb / XST) - 1) & 1, ab)) break;
+        if (kb >= xst && !mbar_wait(&x_empty[sx], ((kb / xst) - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(&x_full[sx], (uint32_t)args.xbytes);
         tma_load_3d(sm + L.xs + sx * args.xbytes, &xmap, &x_full[sx], p0, kb * BK, b);
         ++nx;
@@ -206,8 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++nb;
       }
       // Never leave with a copy in flight.
-      for (int kb = (nx > XST ? nx - XST : 0); kb < nx; ++kb)
-        mbar_wait_drain(&x_full[kb % XST], (kb / XST) & 1, drain_limit(ab));
+      for (int kb = (nx > xst ? nx - xst : 0); kb < nx; ++kb)
+        mbar_wait_drain(&x_full[kb % xst], (kb / xst) & 1, drain_limit(ab));
       for (int kb = (nb > ST ? nb - ST : 0); kb < nb; ++kb)
         mbar_wait_drain(&b_full[kb % ST], (kb / ST) & 1, drain_limit(ab));
     }
@@ -263,11 +264,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     float a_cur = c < args.C ? __ldg(ga + c) : 0.f;
     float s_cur = c < args.C ? __ldg(gs + c) : 0.f;
     for (int kb = 0; kb < nk && ok; ++kb) {
-      const int sx = kb % XST, s = kb % ST;
+      const int sx = kb % xst, s = kb % ST;
       c = (kb + 1) * BK + hc * 32 + lane;
       const float a_nxt = (kb + 1 < nk && c < args.C) ? __ldg(ga + c) : 0.f;
       const float s_nxt = (kb + 1 < nk && c < args.C) ? __ldg(gs + c) : 0.f;
-      if (!mbar_wait_warp(&x_full[sx], (kb / XST) & 1, ab)) { ok = false; break; }
+      if (!mbar_wait_warp(&x_full[sx], (kb / xst) & 1, ab)) { ok = false; break; }
       if (kb >= ST && !mbar_wait_warp(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) { ok = false; break; }
       __syncwarp();
       slot[lane] = a_cur;
@@ -280,6 +281,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int ch0 = hc * 32 + j * 8;     // channel within the k-block
+        // the 8 channels' scale and shift as four 16-byte broadcast loads
+        const float4 a0 = reinterpret_cast<const float4 *>(slot)[2 * j];
+        const float4 a1 = reinterpret_cast<const float4 *>(slot)[2 * j + 1];
+        const float4 s0 = reinterpret_cast<const float4 *>(slot + 32)[2 * j];
+        const float4 s1 = reinterpret_cast<const float4 *>(slot + 32)[2 * j + 1];
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
         float z[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const unsigned short u = reinterpret_cast<const unsigned short *>(xs)[(ch0 + i) * BM + px];
             xv = __uint_as_float(((uint32_t)u) << 16);
           }
-          z[i] = fmaf(slot[j * 8 + i], xv, slot[32 + j * 8 + i]);
+          z[i] = fmaf(av[i], xv, sv[i]);
         }
         st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_op2(z[0], z[1]),
                      pack_op2(z[2], z[3]), pack_op2(z[4], z[5]), pack_op2(z[6], z[7]));
@@ -976,7 +984,13 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
   a.xbytes = BM * BK * es;
   a.ga = ga; a.gs = gs; a.bias = b_qkv; a.q = q; a.k = k; a.vt = vt;
   a.err = kp.err; a.timeout_ns = kp.timeout_ns;
-  const uint32_t smem = smem_total(a.xbytes, BN);
+  // x stages: as many as fit (up to 4), so x loads run ahead of the
+  // conversion instead of waiting for it two blocks back.
+  int max_smem_q = 232448;
+  cudaDeviceGetAttribute(&max_smem_q, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  a.xst = XST;
+  while (a.xst > 2 && (int)smem_total(a.xbytes, BN, a.xst) > max_smem_q) --a.xst;
+  const uint32_t smem = smem_total(a.xbytes, BN, a.xst);
   const dim3 grid(dm.ntot / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(qkv_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
