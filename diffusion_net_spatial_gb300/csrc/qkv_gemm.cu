@@ -199,7 +199,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (args.stall && (uint32_t)(nx + nb) >= args.stall) break;  // test hook: consumers' waits expire
         if (kb >= xst && !mbar_wait(&x_empty[sx], ((kb / xst) - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(&x_full[sx], (uint32_t)args.xbytes);
-        tma_load_3d(sm + L.xs + sx * args.xbytes, &xmap, &x_full[sx], p0, kb * BK, b);
+        // [64 channels][128 pixels] as 128-byte-wide swizzled boxes of
+        // 128 / sizeof(x) pixels (8 KB each)
+        for (int u = 0; u < (DT == 0 ? 4 : 2); ++u)
+          tma_load_3d(sm + L.xs + sx * args.xbytes + u * 8192, &xmap, &x_full[sx], p0 + u * (DT == 0 ? 32 : 64),
+                      kb * BK, b);
         ++nx;
         if (kb >= ST && !mbar_wait(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) break;
         mbar_arrive_expect_tx(&b_full[s], (uint32_t)(args.BN * BK * 2));
@@ -251,58 +255,70 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ converters
+    // Warp cw converts the k-block's channels 8 cw .. 8 cw + 7 for all 128
+    // pixels; thread t owns channel 8 cw + t / 4 and, in each 8-pixel group,
+    // the pixel pair 2 (t % 4), +1: it reads the pair with one load from the
+    // swizzled x stage (the 8 channels of a load sit in 8 different 16-byte
+    // bank groups) and writes the transposed A tile with stmatrix.trans, four
+    // 8 x 8 pixel-by-channel blocks per instruction.
     const int cw = warp - 2;                 // 0..7
-    const int px = (cw & 3) * 32 + lane;     // pixel row of the A tile
-    const int hc = cw >> 2;                  // channel half of the k-block
+    const int cl = cw * 8 + (lane >> 2);     // this thread's channel within the k-block
     float *slot = reinterpret_cast<float *>(sm + L.slot + cw * 256);
+    (void)slot;
     const float *ga = args.ga + (long long)b * args.C;
     const float *gs = args.gs + (long long)b * args.C;
     bool ok = true;
+    // x stage offset of this thread's pixel pair in 8-pixel group T: box
+    // T / (boxes of 128 bytes), 16-byte chunk XOR the channel's row phase.
+    constexpr int ES = DT == 0 ? 4 : 2;
+    constexpr int PPB = 128 / ES;            // pixels per 128-byte box row
+    auto x_off = [&](int T) -> uint32_t {
+      const int px0 = 8 * T + 2 * (lane & 3);
+      const int bx = px0 / PPB, pb = (px0 % PPB) * ES;
+      return (uint32_t)(bx * 8192 + cl * 128 + ((((pb >> 4) ^ (cl & 7)) << 4) | (pb & 15)));
+    };
+    // stmatrix row addresses: matrix i = lane / 8 (pixel group 4 g + i), row
+    // lane % 8 (its pixel), chunk cw (this warp's 8 channels).
+    const int prow = 8 * (lane >> 3) + (lane & 7);  // + 32 g
     // The GN scale/shift of the next k-block are fetched one iteration ahead,
     // so their global-memory latency overlaps the current block.
-    int c = hc * 32 + lane;
+    int c = cl;
     float a_cur = c < args.C ? __ldg(ga + c) : 0.f;
     float s_cur = c < args.C ? __ldg(gs + c) : 0.f;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int sx = kb % xst, s = kb % ST;
-      c = (kb + 1) * BK + hc * 32 + lane;
+      c = (kb + 1) * BK + cl;
       const float a_nxt = (kb + 1 < nk && c < args.C) ? __ldg(ga + c) : 0.f;
       const float s_nxt = (kb + 1 < nk && c < args.C) ? __ldg(gs + c) : 0.f;
       if (!mbar_wait_warp(&x_full[sx], (kb / xst) & 1, ab)) { ok = false; break; }
       if (kb >= ST && !mbar_wait_warp(&ab_empty[s], ((kb / ST) - 1) & 1, ab)) { ok = false; break; }
-      __syncwarp();
-      slot[lane] = a_cur;
-      slot[32 + lane] = s_cur;
+      const uint32_t xs = smem_u32(sm + L.xs + sx * args.xbytes);
+      const uint32_t a_tile = smem_u32(sm + L.as + s * (BM * BK * 2));
+      // channels past C are zero (their scale and shift are zero)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t off = x_off(4 * g + i);
+          float x0, x1;
+          if (DT == 0) {
+            float2 v;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(xs + off));
+            x0 = v.x;
+            x1 = v.y;
+          } else {
+            uint32_t v;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(xs + off));
+            x0 = __uint_as_float(v << 16);
+            x1 = __uint_as_float(v & 0xFFFF0000u);
+          }
+          w[i] = pack_op2(fmaf(a_cur, x0, s_cur), fmaf(a_cur, x1, s_cur));
+        }
+        stmatrix_x4_trans(a_tile + sw128_offset((uint32_t)(32 * g + prow), (uint32_t)cw), w[0], w[1], w[2], w[3]);
+      }
       a_cur = a_nxt;
       s_cur = s_nxt;
-      __syncwarp();
-      const uint8_t *xs = sm + L.xs + sx * args.xbytes;
-      const uint32_t a_tile = smem_u32(sm + L.as + s * (BM * BK * 2));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch0 = hc * 32 + j * 8;     // channel within the k-block
-        // the 8 channels' scale and shift as four 16-byte broadcast loads
-        const float4 a0 = reinterpret_cast<const float4 *>(slot)[2 * j];
-        const float4 a1 = reinterpret_cast<const float4 *>(slot)[2 * j + 1];
-        const float4 s0 = reinterpret_cast<const float4 *>(slot + 32)[2 * j];
-        const float4 s1 = reinterpret_cast<const float4 *>(slot + 32)[2 * j + 1];
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        float z[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float xv;
-          if (DT == 0) {
-            xv = reinterpret_cast<const float *>(xs)[(ch0 + i) * BM + px];
-          } else {
-            const unsigned short u = reinterpret_cast<const unsigned short *>(xs)[(ch0 + i) * BM + px];
-            xv = __uint_as_float(((uint32_t)u) << 16);
-          }
-          z[i] = fmaf(av[i], xv, sv[i]);
-        }
-        st_shared_v4(a_tile + sw128_offset((uint32_t)px, (uint32_t)(ch0 >> 3)), pack_op2(z[0], z[1]),
-                     pack_op2(z[2], z[3]), pack_op2(z[4], z[5]), pack_op2(z[6], z[7]));
-      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -884,6 +900,15 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
       return 1;
   }
   const int BN = pick_bn(dm.ntot);
+  CUtensorMap xmap_g;  // the general kernel's x stage: 128-byte-wide swizzled boxes
+  {
+    const uint64_t dims[3] = {(uint64_t)dm.N, (uint64_t)dm.C, (uint64_t)dm.B};
+    const uint64_t strides[2] = {(uint64_t)ldx * es, (uint64_t)dm.C * ldx * es};
+    const uint32_t box[3] = {(uint32_t)(128 / es), BK, 1};
+    if (encode_tiled(&xmap_g, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return 1;
+  }
   {
     const uint64_t dims[2] = {(uint64_t)dm.C, (uint64_t)dm.ntot};
     const uint64_t strides[1] = {(uint64_t)dm.ldc * 2};
@@ -994,10 +1019,10 @@ int launch_qkv_gemm(const Dims &dm, int dtype, const void *x, int ldx, const flo
   const dim3 grid(dm.ntot / BN, (dm.N + BM - 1) / BM, dm.B);
   if (dtype == 0) {
     cudaFuncSetAttribute(qkv_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    (void)launch_k(qkv_gemm_kernel<0>, dim3(grid), dim3(THREADS), smem, st, xmap, wmap, qmap, kmap, vmap, a);
+    (void)launch_k(qkv_gemm_kernel<0>, dim3(grid), dim3(THREADS), smem, st, xmap_g, wmap, qmap, kmap, vmap, a);
   } else {
     cudaFuncSetAttribute(qkv_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    (void)launch_k(qkv_gemm_kernel<1>, dim3(grid), dim3(THREADS), smem, st, xmap, wmap, qmap, kmap, vmap, a);
+    (void)launch_k(qkv_gemm_kernel<1>, dim3(grid), dim3(THREADS), smem, st, xmap_g, wmap, qmap, kmap, vmap, a);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

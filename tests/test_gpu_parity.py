@@ -152,7 +152,11 @@ def _step_inputs(ssa, wl):
 
 
 STEP_SHAPES = [("d64", 2, 128, 12, 20, 8, 2, "f32"), ("d40", 1, 80, 16, 8, 8, 2, "f32"),
-               ("d512", 1, 512, 8, 32, 32, 1, "f32"), ("bf16", 2, 256, 8, 8, 16, 4, "bf16")]
+               ("d512", 1, 512, 8, 32, 32, 1, "f32"), ("bf16", 2, 256, 8, 8, 16, 4, "bf16"),
+               # C > 512: the general projection (fp32 x: four 32-pixel x boxes per stage) and
+               # out-projection kernels; N = 208 leaves a ragged second pixel tile
+               ("c640-f32", 2, 640, 13, 16, 32, 10, "f32"),
+               ("c1280-bf16", 1, 1280, 12, 12, 32, 20, "bf16")]
 
 
 @pytest.mark.parametrize("case", STEP_SHAPES, ids=[c[0] for c in STEP_SHAPES])
