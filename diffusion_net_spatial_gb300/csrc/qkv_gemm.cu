@@ -480,8 +480,10 @@ constexpr uint32_t RES_SMEM = RES_BARS_OFF + RNBARS * 8 + 16;
 // `bl`: lane l holds the bias of the chunk's column l (fetched by the caller
 // before its wait for the accumulator), handed to every lane by shuffles.
 template <int CW>
-__device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t taddr, int F0, int b, int p0, int q4,
-                                              int lane, const float2 *th, float bl) {
+// (sec, hd, r0): section (Q, K, V), head and packed row inside the head of the
+// chunk's first column F0, kept by the caller without divisions.
+__device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t taddr, int F0, int sec, int hd, int r0,
+                                              int b, int p0, int q4, int lane, const float2 *th, float bl) {
   uint32_t r[CW];
   if constexpr (CW == 32) tmem_ld32(taddr, r);
   else tmem_ld16(taddr, r);
@@ -489,10 +491,7 @@ __device__ __forceinline__ void res_epi_chunk(const ResArgs &args, uint32_t tadd
   float v[CW];
 #pragma unroll
   for (int k = 0; k < CW; ++k) v[k] = __uint_as_float(r[k]) + __shfl_sync(0xFFFFFFFFu, bl, k);
-  const int hdp = args.h * args.dp;
-  const int sec = F0 / hdp;
-  const int hd = (F0 / args.dp) % args.h;
-  const int r0 = F0 % args.dp;  // packed row of the chunk's first column inside its head
+  (void)F0;
   const int row = q4 * 32 + lane;
   const int pix = p0 + row;
   if (sec == 2) {
@@ -840,12 +839,30 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       if (!mbar_wait_warp(&acc_full[buf], (uint32_t)((i >> 1) & 1), ab)) { ok = false; break; }
       tc_fence_after();
       const uint32_t acc = lane_base + (uint32_t)(buf * 128);
+      // Section, head and row of this warp's first chunk, then advanced by
+      // two chunks at a time (no integer division per chunk).
+      int F0 = fs + hc * args.cw;
+      int ec = F0 / args.dp;
+      int er0 = F0 - ec * args.dp;
+      int esec = ec / args.h;
+      int ehd = ec - esec * args.h;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = hc + 2 * u;
         if (c >= nch) break;
-        if (args.cw == 32) res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), fs + c * 32, b, p0, q4, lane, th, bl[u]);
-        else res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), fs + c * 16, b, p0, q4, lane, th, bl[u]);
+        if (args.cw == 32)
+          res_epi_chunk<32>(args, acc + (uint32_t)(c * 32), F0, esec, ehd, er0, b, p0, q4, lane, th, bl[u]);
+        else
+          res_epi_chunk<16>(args, acc + (uint32_t)(c * 16), F0, esec, ehd, er0, b, p0, q4, lane, th, bl[u]);
+        F0 += 2 * args.cw;
+        er0 += 2 * args.cw;
+        while (er0 >= args.dp) {
+          er0 -= args.dp;
+          if (++ehd == args.h) {
+            ehd = 0;
+            ++esec;
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
