@@ -156,7 +156,9 @@ STEP_SHAPES = [("d64", 2, 128, 12, 20, 8, 2, "f32"), ("d40", 1, 80, 16, 8, 8, 2,
                # C > 512: the general projection (fp32 x: four 32-pixel x boxes per stage) and
                # out-projection kernels; N = 208 leaves a ragged second pixel tile
                ("c640-f32", 2, 640, 13, 16, 32, 10, "f32"),
-               ("c1280-bf16", 1, 1280, 12, 12, 32, 20, "bf16")]
+               ("c1280-bf16", 1, 1280, 12, 12, 32, 20, "bf16"),
+               # C = 544: the last 64-channel k-block is half past C (zero-filled x, zero scale)
+               ("c544-f32", 1, 544, 9, 12, 32, 8, "f32")]
 
 
 @pytest.mark.parametrize("case", STEP_SHAPES, ids=[c[0] for c in STEP_SHAPES])
