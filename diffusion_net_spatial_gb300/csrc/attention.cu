@@ -4,9 +4,11 @@
 // channels in head order; worked example 1 divides the scores by sqrt(2) for
 // d = 2).
 //
-// Flash-style: one CTA owns 128 queries of one (sample, head) -- and one of
+// Flash-style, the N x N score matrix never exists.  In the single and
+// double modes one CTA owns 128 queries of one (sample, head) -- and one of
 // the two output halves when the padded head dim exceeds 256 -- and walks the
-// keys in tiles of 128, so the N x N score matrix never exists.
+// keys in tiles of 128 (the quad and pair modes are described at their
+// kernels):
 //   warp 0     TMA producer: Q once, then K and V^T through a ring of slots
 //              (16 KB with two CTAs per SM, 32 KB with one) of 128-byte
 //              swizzled, K-major boxes: K as [128 keys x 64 dims] per 16 KB,
@@ -20,7 +22,11 @@
 //              rescaled in tensor memory) when it grows by more than 2^8,
 //              which keeps every P <= 256 and is exact after the final
 //              division by the row sum.
-// Three modes:
+// Four modes:
+//   quad    padded head dim <= 64 without the causal mask (the table only
+//           when W % 32 == 0): 64-key tiles, P written over its scores, 128
+//           tensor-memory columns per query tile, four query tiles per SM
+//           (described at attention_quad_kernel).
 //   single  S uses 128 tensor-memory columns; the MMA writes S_{j+1} as soon
 //           as the softmax warps have read S_j.  With a small head dim this
 //           fits 256 columns and ~113 KB of shared memory, so two CTAs share
