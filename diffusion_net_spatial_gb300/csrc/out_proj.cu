@@ -178,12 +178,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c16 = half; c16 < BN / 16; c16 += 2) {
           uint32_t r[16];
           tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(c16 * 16), r);
+          // the chunk's biases, loaded while the accumulator load is in flight
+          float bv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = n0 + c16 * 16 + i;
+            bv[i] = c < args.C ? __ldg(args.bias + c) : 0.f;
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int cl = c16 * 16 + i;
-            const int c = n0 + cl;
-            const float bias = c < args.C ? __ldg(args.bias + c) : 0.f;
+            const float bias = bv[i];
             if (DT == 0) {
               float *px = reinterpret_cast<float *>(xs) + cl * BM + row;
               *px = *px + (__uint_as_float(r[i]) + bias);
