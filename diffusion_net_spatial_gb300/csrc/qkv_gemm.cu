@@ -263,8 +263,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // 8 x 8 pixel-by-channel blocks per instruction.
     const int cw = warp - 2;                 // 0..7
     const int cl = cw * 8 + (lane >> 2);     // this thread's channel within the k-block
-    float *slot = reinterpret_cast<float *>(sm + L.slot + cw * 256);
-    (void)slot;
     const float *ga = args.ga + (long long)b * args.C;
     const float *gs = args.gs + (long long)b * args.C;
     bool ok = true;
@@ -334,9 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // which clips pixels past N.  With pair-interleaved Q/K rows a chunk holds
     // 8 pairs (features i0..i0+7 and d/2+i0..d/2+i0+7): it is staged as two
     // [128 pixels][8] halves, rotated first when the rotary embedding is on.
-    float2 *th = reinterpret_cast<float2 *>(sm + L.slot);  // rotation thetas (the x staging slots are idle now)
+    float2 *th = reinterpret_cast<float2 *>(sm + L.slot);  // rotation thetas (in the otherwise unused slot area)
     if (args.rope) {
-      named_bar_sync(1, NCONV * 32);  // every converter is done with its slot
+      named_bar_sync(1, NCONV * 32);  // every converter has left its k-block loop
       rope_thetas(th, args.d, threadIdx.x - 64, NCONV * 32);
       named_bar_sync(1, NCONV * 32);
     }
