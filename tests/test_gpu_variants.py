@@ -66,6 +66,7 @@ SHAPES = [
     ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
     ("d64-w32", 1, 128, 6, 32, 8, 2, "f32"),  # quad, W % 32 == 0: the table path; N = 192 (ragged tile)
     ("d40-w64", 1, 80, 3, 64, 8, 2, "f32"),   # quad with the ones column, W = 64
+    ("d64-n320", 1, 128, 16, 20, 8, 2, "f32"),  # quad, 3 query tiles: the second CTA's second tile is past N
 ]
 VARIANTS = ["no_bias", "causal", "rope", "rel", "causal_rel", "qk_norm", "qk_norm_rope", "all"]
 
