@@ -198,6 +198,41 @@ def test_qkv_attention_outproj_steps(ssa, case):
     assert np.linalg.norm(got - out_ref) / np.linalg.norm(y_ref) < 2e-3
 
 
+# The resident out-projection (C <= 512, at least 64 pixel tiles): one CTA per
+# 128-pixel tile; once its MMAs are done it streams the residual through as many
+# 128-channel buffers as the freed shared memory holds.  C = 512 fp32 takes three
+# (the fourth piece reloads the first buffer), bf16 four, C = 384 fp32 three.
+OUTPROJ_RESIDENT = [("c512-f32", 1, 512, 64, 128, "f32"),
+                    ("c512-bf16", 1, 512, 64, 128, "bf16"),
+                    ("c384-f32-b2", 2, 384, 64, 64, "f32"),
+                    ("c512-f32-ragged", 1, 512, 90, 92, "f32")]   # 65 tiles, the last one 88 pixels
+
+
+@pytest.mark.parametrize("case", OUTPROJ_RESIDENT, ids=[c[0] for c in OUTPROJ_RESIDENT])
+def test_out_projection_resident(ssa, case):
+    """The out-projection step alone, on a seeded O in [-1, 1), against the
+    oracle's projection plus residual."""
+    name, B, C, H, W, dt = case
+    h = C // 64
+    wl = wls.custom(name, B, C, H, W, 32, h, dt, seed=31)
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    pk = ssa.ssa_pack_weights(pd, h)
+    N, ldc = H * W, ssa.layout(B, C, H, W, h)["ldc"]
+    g = torch.Generator().manual_seed(37)
+    o_cpu = (torch.rand(B, N, ldc, generator=g) * 2 - 1).to(torch.float16)
+    out = ssa.ssa_out_project(o_cpu.to(xd.device), pk["w_o"], pk["b_o"], xd)
+    assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+    og = o_cpu[..., :C].double().numpy()
+    y_ref = oracle.out_proj(og, p["out_weight"], p["out_bias"])
+    xs = x.double().numpy().reshape(B, C, N)
+    out_ref = oracle.round_to(xs + y_ref, dt)
+    out_ref = oracle.bf16_bits_to_f64(out_ref) if dt == "bf16" else out_ref.astype(np.float64)
+    got = out.double().cpu().numpy().reshape(B, C, N)
+    assert np.linalg.norm(got - out_ref) / np.linalg.norm(y_ref) < 2e-3
+    assert np.abs(got - out_ref).max() < 5e-2
+
+
 def test_timeout_path_returns_status_and_context_survives(ssa):
     """A wait that nothing ends expires after its limit, latches
     SSA_ERR_TIMEOUT, and the context stays usable."""
