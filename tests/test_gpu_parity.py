@@ -121,6 +121,40 @@ def test_planned_matches_one_shot_bitwise(ssa):
     plan.close()
 
 
+@pytest.mark.parametrize("name", ["unet-l1", "vae1024", "unet-lowres"])
+def test_planned_forward_in_a_cuda_graph(ssa, name):
+    """With its output and workspace given, a planned forward issues only
+    stream-ordered work (no host synchronisation, no allocation), so it can be
+    captured into a CUDA graph; every replay matches a direct call bit for bit.
+    unet-l1 runs the quad attention mode, vae1024 the pair mode with its work
+    split (a counter memset in the graph), unet-lowres bf16 x."""
+    wl = wls.WORKLOADS[name]
+    x, p, _ = wls.make_inputs(wl)
+    xd, pd = _to_dev(x, p)
+    plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads)
+    ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=xd.device)
+    ref = plan.forward(xd, workspace=ws)
+    assert ssa.ssa_get_device_status() == 0
+    out = torch.empty_like(xd)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.forward(xd, out=out, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.forward(xd, out=out, workspace=ws, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+        assert torch.equal(out, ref)
+    del g
+    plan.close()
+
+
 def test_gn_stats_step(ssa):
     """GN statistics kernel against the oracle's two-pass fp64 statistics."""
     for (B, C, H, W, G, dt, shift) in [(2, 320, 64, 64, 32, "f32", 0.0), (1, 512, 128, 128, 32, "f32", 3.0),
