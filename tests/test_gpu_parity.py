@@ -155,6 +155,36 @@ def test_planned_forward_in_a_cuda_graph(ssa, name):
     plan.close()
 
 
+def test_two_plans_on_two_streams(ssa):
+    """Plans share no device state but the status word: two shapes (quad-mode
+    unet-l1, split pair-mode vae1024) run concurrently on two streams, several
+    times over, give exactly their results run alone."""
+    runs = []
+    for name in ("unet-l1", "vae1024"):
+        wl = wls.WORKLOADS[name]
+        x, p, _ = wls.make_inputs(wl)
+        xd, pd = _to_dev(x, p)
+        plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads)
+        ws = torch.empty(plan.workspace_size(wl.B, wl.H, wl.W), dtype=torch.uint8, device=xd.device)
+        ref = plan.forward(xd, workspace=ws)
+        runs.append((plan, xd, ws, ref, torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    assert ssa.ssa_get_device_status() == 0
+    outs = [torch.empty_like(r[1]) for r in runs]
+    for _ in range(4):
+        for (plan, xd, ws, _, st), out in zip(runs, outs):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                out.zero_()
+                plan.forward(xd, out=out, workspace=ws, stream=st)
+        torch.cuda.synchronize()
+        assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+        for (_, _, _, ref, _), out in zip(runs, outs):
+            assert torch.equal(out, ref)
+    for r in runs:
+        r[0].close()
+
+
 def test_gn_stats_step(ssa):
     """GN statistics kernel against the oracle's two-pass fp64 statistics."""
     for (B, C, H, W, G, dt, shift) in [(2, 320, 64, 64, 32, "f32", 0.0), (1, 512, 128, 128, 32, "f32", 3.0),
