@@ -37,9 +37,10 @@ __global__ void rope_kernel(uint16_t *q, uint16_t *k, int total, int N, int ldq,
   for (int i = threadIdx.x; i < hd; i += blockDim.x) theta[i] = exp2f(l2base * (float)i);
   __syncthreads();
   pdl_wait();
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
-    const int row = idx / hd;
-    const int i = idx - row * hd;
+  // Unsigned: total < 2^31 and the stride <= 2^20, so idx + stride never wraps.
+  for (unsigned idx = blockIdx.x * blockDim.x + threadIdx.x; idx < (unsigned)total; idx += gridDim.x * blockDim.x) {
+    const int row = (int)(idx / (unsigned)hd);
+    const int i = (int)idx - row * hd;
     const float t = (float)(row % N);
     float sn, cs;
     sincosf(t * theta[i], &sn, &cs);

@@ -102,6 +102,38 @@ def test_block_named_workloads(ssa, name):
     assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
 
 
+def test_block_past_2_31_elements(ssa):
+    """B*C*N = 32767 * 1024 * 72 = 2.4e9 elements (> 2^31), a shape the shape
+    checks admit (B*h = 65534 head tiles): every kernel's offsets past 32 bits,
+    the general projection (C > 512) and the split d = 512 attention.  x is
+    drawn on the device; three samples against the oracle, all of out finite."""
+    B, C, H, W, G, h = 32767, 1024, 8, 9, 1, 2
+    free, _ = torch.cuda.mem_get_info()
+    if free < (48 << 30):
+        pytest.skip("needs ~45 GB of free device memory")
+    _, p, _ = wls.make_inputs(wls.custom("big", 1, C, H, W, G, h, "f32", seed=41))
+    dev = torch.device("cuda:0")
+    pd = {k: v.to(dev) for k, v in p.items()}
+    gen = torch.Generator(device=dev).manual_seed(43)
+    xd = torch.randn((B, C, H, W), generator=gen, device=dev, dtype=torch.float32)
+    plan = ssa.SsaPlan(pd, G, h)
+    try:
+        out = plan.forward(xd)
+        assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+        for b in (0, 12345, B - 1):
+            xb = xd[b:b + 1].cpu()
+            ref, y = oracle.block(xb, p, G, h)
+            got = out[b:b + 1].double().cpu().numpy().reshape(1, C, -1)
+            rel = np.linalg.norm(got - ref) / max(np.linalg.norm(y), 1e-30)
+            mx = np.abs(got - ref).max()
+            assert rel <= REL_L2 and mx <= MAX_ABS, (b, rel, mx)
+        assert bool(torch.isfinite(out).all())
+    finally:
+        plan.close()
+        del xd
+        torch.cuda.empty_cache()
+
+
 def test_in_place(ssa):
     wl = wls.custom("inplace", 2, 128, 8, 16, 8, 2, "f32", seed=5)
     rel, mx = _run(ssa, wl, inplace=True)
