@@ -97,6 +97,34 @@ def test_variant_parity(ssa, name, B, C, H, W, G, h, dt, variant):
     _check(ssa, out, x, p, wl, **okw)
 
 
+def test_rope_pass_near_2_31_pairs(ssa):
+    """The separate rotary pass (it follows the query-key norm) over
+    B*h*N*d/2 = 65534 * 128 * 256 = 2,147,418,112 pairs: within 2^20 of 2^31,
+    where a 32-bit grid-stride index would wrap.  x is drawn on the device;
+    three samples against the oracle, all of out finite."""
+    B, C, H, W, G, h = 32767, 1024, 8, 16, 1, 2
+    free, _ = torch.cuda.mem_get_info()
+    if free < (80 << 30):
+        pytest.skip("needs ~70 GB of free device memory")
+    wl, _, p, _ = _inputs(1, C, H, W, G, h, "f32", seed=47)
+    qg, kg = p.pop("_qg"), p.pop("_kg")
+    dev = torch.device("cuda:0")
+    pd = {k: v.to(dev) for k, v in p.items()}
+    gen = torch.Generator(device=dev).manual_seed(53)
+    xd = torch.randn((B, C, H, W), generator=gen, device=dev, dtype=torch.float32)
+    try:
+        out = ssa.ssa_forward(xd, pd, G, h, rope=True, q_norm_weight=qg.to(dev), k_norm_weight=kg.to(dev))
+        assert ssa.ssa_get_device_status() == 0, ssa.ssa_last_error_string()
+        for b in (0, 20000, B - 1):
+            xb = xd[b:b + 1].cpu()
+            _check(ssa, out[b:b + 1], xb, p, wl, rope=True, q_norm_weight=qg.double().numpy(),
+                   k_norm_weight=kg.double().numpy())
+        assert bool(torch.isfinite(out).all())
+    finally:
+        del xd
+        torch.cuda.empty_cache()
+
+
 def test_planned_variants_match_one_shot(ssa):
     wl, x, p, rel = _inputs(2, 128, 10, 14, 8, 4, "f32", seed=5)
     qg, kg = p.pop("_qg").cuda(), p.pop("_kg").cuda()
