@@ -104,6 +104,16 @@ ssa_status check_shape(int B, int C, int H, int W, int G, int h) {
   return SSA_OK;
 }
 
+// The relative-position table of an H x W grid has (2H-1)(2W-1) entries per
+// head, counted and indexed in 32 bits by the table kernels.
+ssa_status check_rel_grid(int H, int W) {
+  const long long entries = (2LL * H - 1) * (2LL * W - 1);
+  if (entries > 2147483647LL)
+    return fail(SSA_ERR_UNSUPPORTED, "a relative-position table of %lld entries per head (grid %d x %d) exceeds 2^31 - 1",
+                entries, H, W);
+  return SSA_OK;
+}
+
 ssa_status check_dtype(ssa_dtype dt) {
   if (dt != SSA_F32 && dt != SSA_BF16) return fail(SSA_ERR_DTYPE, "dtype %d is neither SSA_F32 nor SSA_BF16", (int)dt);
   return SSA_OK;
@@ -182,6 +192,10 @@ struct Variants {
 ssa_status check_variants(const Dims &dm, const Variants &v) {
   if (v.rope && dm.d % 2) return fail(SSA_ERR_CONSTRAINT, "rope needs an even head dim (d = %d)", dm.d);
   if (v.rel_table && !aligned16(v.rel_table)) return fail(SSA_ERR_ALIGNMENT, "rel_pos_table must be 16-byte aligned");
+  if (v.rel_table) {
+    const ssa_status s = check_rel_grid(dm.H, dm.W);
+    if (s != SSA_OK) return s;
+  }
   if ((v.q_gamma == nullptr) != (v.k_gamma == nullptr))
     return fail(SSA_ERR_NULL, "q_norm_weight and k_norm_weight must be given together");
   return SSA_OK;
@@ -615,6 +629,7 @@ ssa_status ssa_pack_rel_table(const void *table, ssa_dtype dtype, int H, int W, 
   if (H <= 0 || W <= 0 || num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "sizes must be positive");
   ssa_status s = check_dtype(dtype);
   if (s != SSA_OK) return s;
+  if ((s = check_rel_grid(H, W)) != SSA_OK) return s;
   if (!table || !packed) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if ((s = device_state(nullptr, nullptr)) != SSA_OK) return s;
   const cudaError_t e = launch_rel_table_pack((int)dtype, table, H, W, num_heads, packed,
@@ -630,6 +645,7 @@ ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t
   if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
     return fail(SSA_ERR_ALIGNMENT, "q, k, vt and o must be 16-byte aligned");
+  if (rel_packed && (s = check_rel_grid(H, W)) != SSA_OK) return s;
   KParams kp{};
   int num_sms = 0;
   if ((s = kparams(&kp, &num_sms)) != SSA_OK) return s;
@@ -649,6 +665,7 @@ ssa_status ssa_attention_ws(const uint16_t *q, const uint16_t *k, const uint16_t
   if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
     return fail(SSA_ERR_ALIGNMENT, "q, k, vt and o must be 16-byte aligned");
+  if (rel_packed && (s = check_rel_grid(H, W)) != SSA_OK) return s;
   const Dims dm = make_dims(B, C, H, W, 1, num_heads);
   const size_t need = attention_scratch_bytes(dm);
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
