@@ -29,7 +29,9 @@ namespace {
 // One thread per (row, pair i), consecutive threads on consecutive pairs of a
 // row; the angle bases theta_i = 10000^(-2i/d) come from a table each block
 // builds once in shared memory, and the index arithmetic is 32-bit.
-__global__ void rope_kernel(uint16_t *q, uint16_t *k, int total, int N, int ldq, int d) {
+// t0: the token position of row 0 of this launch (launches cover chunks of
+// rows, so that total < 2^31).
+__global__ void rope_kernel(uint16_t *q, uint16_t *k, int total, int N, int ldq, int d, int t0) {
   __shared__ float theta[256];
   pdl_trigger();
   const int hd = d / 2;
@@ -41,7 +43,7 @@ __global__ void rope_kernel(uint16_t *q, uint16_t *k, int total, int N, int ldq,
   for (unsigned idx = blockIdx.x * blockDim.x + threadIdx.x; idx < (unsigned)total; idx += gridDim.x * blockDim.x) {
     const int row = (int)(idx / (unsigned)hd);
     const int i = (int)idx - row * hd;
-    const float t = (float)(row % N);
+    const float t = (float)((row + t0) % N);
     float sn, cs;
     sincosf(t * theta[i], &sn, &cs);
     uint16_t *pq = q + (long long)row * ldq;
@@ -68,8 +70,10 @@ __device__ __forceinline__ float ld_x(const void *p, long long i) {
 // elements j, j + 8, ...; the sum of squares is combined by shuffles inside
 // the group of eight and the row is scaled on a second read (from L1).
 template <int DT>
+// hd0: the head of row 0 of this launch (launches cover chunks of whole
+// heads' rows, so that 16 * rows < 2^31).
 __global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, int rows, int N, int h, int ldq, int d, const void *qg,
-                               const void *kg) {
+                               const void *kg, int hd0) {
   pdl_trigger();
   pdl_wait();
   const int wr = (blockIdx.x * blockDim.x + threadIdx.x) >> 3;  // uniform within a group of eight lanes
@@ -78,7 +82,7 @@ __global__ void qk_norm_kernel(uint16_t *q, uint16_t *k, int rows, int N, int h,
   const unsigned gmask = 0xFFu << (threadIdx.x & 24);
   const int which = wr >= rows ? 1 : 0;
   const int row = wr - which * rows;
-  const int head = (row / N) % h;
+  const int head = (hd0 + row / N) % h;
   uint16_t *p = (which ? k : q) + (long long)row * ldq;
   const void *g = which ? kg : qg;
   const long long g0 = (long long)head * d;
@@ -152,23 +156,37 @@ int grid_for(long long work) {
 }  // namespace
 
 cudaError_t launch_rope(const Dims &dm, uint16_t *q, uint16_t *k, cudaStream_t st) {
-  const long long total = (long long)dm.B * dm.h * dm.N * (dm.d / 2);
-  if (dm.d / 2 > 256 || total >= (1LL << 31)) return cudaErrorInvalidValue;
-  (void)launch_k(rope_kernel, dim3(grid_for(total)), dim3(256), 0, st, q, k, (int)total, dm.N, dm.ldq, dm.d);
+  const int hd = dm.d / 2;
+  if (hd <= 0 || hd > 256) return cudaErrorInvalidValue;
+  // Chunks of at most 2^30 pairs (whole rows); one launch for all but the
+  // largest problems.
+  const long long rows = (long long)dm.B * dm.h * dm.N;
+  const long long per = (1LL << 30) / hd;
+  for (long long r0 = 0; r0 < rows; r0 += per) {
+    const long long n = rows - r0 < per ? rows - r0 : per;
+    (void)launch_k(rope_kernel, dim3(grid_for(n * hd)), dim3(256), 0, st, q + r0 * dm.ldq, k + r0 * dm.ldq,
+                   (int)(n * hd), dm.N, dm.ldq, dm.d, (int)(r0 % dm.N));
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_qk_norm(const Dims &dm, int dtype, uint16_t *q, uint16_t *k, const void *q_gamma,
                            const void *k_gamma, cudaStream_t st) {
+  // Chunks of whole heads' rows with 16 * rows < 2^31 (one launch for all
+  // but the largest problems): eight lanes per row, Q and K.
   const long long rows = (long long)dm.B * dm.h * dm.N;
-  if (16 * rows >= (1LL << 31)) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)((16 * rows + 127) / 128));  // eight lanes per row, Q and K
-  if (dtype == 0)
-    (void)launch_k(qk_norm_kernel<0>, grid, dim3(128), 0, st, q, k, (int)rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma,
-                   k_gamma);
-  else
-    (void)launch_k(qk_norm_kernel<1>, grid, dim3(128), 0, st, q, k, (int)rows, dm.N, dm.h, dm.ldq, dm.d, q_gamma,
-                   k_gamma);
+  const long long per = ((1LL << 27) - 1) / dm.N * dm.N;  // N <= 2^23 here, so per >= N
+  for (long long r0 = 0; r0 < rows; r0 += per) {
+    const long long n = rows - r0 < per ? rows - r0 : per;
+    const dim3 grid((unsigned)((16 * n + 127) / 128));
+    const int hd0 = (int)((r0 / dm.N) % dm.h);
+    if (dtype == 0)
+      (void)launch_k(qk_norm_kernel<0>, grid, dim3(128), 0, st, q + r0 * dm.ldq, k + r0 * dm.ldq, (int)n, dm.N, dm.h,
+                     dm.ldq, dm.d, q_gamma, k_gamma, hd0);
+    else
+      (void)launch_k(qk_norm_kernel<1>, grid, dim3(128), 0, st, q + r0 * dm.ldq, k + r0 * dm.ldq, (int)n, dm.N, dm.h,
+                     dm.ldq, dm.d, q_gamma, k_gamma, hd0);
+  }
   return cudaGetLastError();
 }
 
