@@ -74,6 +74,7 @@ SMALL = [
     ("d500-b2", 2, 500, 9, 14, 20, 1, "f32"),          # d = 500 (not a multiple of 8): element stores
     ("d16-multihead", 2, 64, 5, 7, 4, 4, "f32"),       # N = 35 (not a multiple of 4: padded-x path)
     ("bf16-d64", 2, 256, 8, 12, 16, 4, "bf16"),
+    ("bf16-n35", 2, 128, 5, 7, 8, 2, "bf16"),         # bf16 x, N = 35: 70-byte rows, the padded-x path
     ("single-pixel", 3, 64, 1, 1, 64, 2, "f32"),       # H = W = 1, one channel per group
     ("group1-head1", 1, 96, 6, 6, 1, 1, "f32"),        # one group, one head (d = 96)
     ("d32-multitile", 1, 64, 16, 24, 8, 2, "f32"),     # N = 384: three key tiles
@@ -134,8 +135,9 @@ def test_block_past_2_31_elements(ssa):
         torch.cuda.empty_cache()
 
 
-def test_in_place(ssa):
-    wl = wls.custom("inplace", 2, 128, 8, 16, 8, 2, "f32", seed=5)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_in_place(ssa, dt):
+    wl = wls.custom("inplace", 2, 128, 8, 16, 8, 2, dt, seed=5)
     rel, mx = _run(ssa, wl, inplace=True)
     assert rel <= REL_L2 and mx <= MAX_ABS
 
