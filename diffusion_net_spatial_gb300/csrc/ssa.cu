@@ -91,12 +91,19 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Checks shared by every entry point that takes the problem shape; a
 // num_groups or num_heads of 0 means "not used by this entry point".
+// An empty problem (B, H or W zero; C and its split into groups and heads
+// still valid) is no work: check_shape returns kEmpty, and every entry point
+// then returns SSA_OK before touching its pointers or the device.
+constexpr ssa_status kEmpty = static_cast<ssa_status>(1000);
+
 ssa_status check_shape(int B, int C, int H, int W, int G, int h) {
-  if (B <= 0 || C <= 0 || H <= 0 || W <= 0 || G < 0 || h < 0)
-    return fail(SSA_ERR_CONSTRAINT, "sizes must be positive (B=%d C=%d H=%d W=%d G=%d h=%d)", B, C, H, W, G, h);
+  if (B < 0 || C <= 0 || H < 0 || W < 0 || G < 0 || h < 0)
+    return fail(SSA_ERR_CONSTRAINT, "sizes must be non-negative, C positive (B=%d C=%d H=%d W=%d G=%d h=%d)", B, C,
+                H, W, G, h);
   if (G > 0 && C % G) return fail(SSA_ERR_CONSTRAINT, "num_groups (%d) must divide C (%d)", G, C);
   if (h > 0 && C % h) return fail(SSA_ERR_CONSTRAINT, "num_heads (%d) must divide C (%d)", h, C);
   if (h > 0 && C / h > 512) return fail(SSA_ERR_UNSUPPORTED, "head dim %d > 512", C / h);
+  if (B == 0 || H == 0 || W == 0) return kEmpty;
   const long long N = (long long)H * W;
   if (N > (1LL << 30) || (long long)B * (G > 0 ? G : 1) > 65535 || (long long)B * (h > 0 ? h : 1) > 65535 ||
       B > 65535 || (N + 127) / 128 > 65535 || (long long)B * C * N > (1LL << 40))
@@ -345,6 +352,7 @@ static ssa_status forward_impl(const void *x, int B, int C, int H, int W, int nu
                                ssa_dtype dtype, const Variants &var, void *workspace, size_t workspace_bytes,
                                void *stream) {
   ssa_status s = check_shape(B, C, H, W, num_groups, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   // Biases may be NULL (that projection has no bias).
@@ -408,6 +416,7 @@ ssa_status ssa_plan_create(ssa_plan **plan, int C, int num_groups, int num_heads
   if (!plan) return fail(SSA_ERR_NULL, "plan out-pointer is NULL");
   *plan = nullptr;
   ssa_status s = check_shape(1, C, 1, 1, num_groups, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   const void *ptrs[] = {norm_weight, norm_bias, q_weight, k_weight, v_weight, out_weight};  // biases may be NULL
@@ -462,6 +471,7 @@ static ssa_status planned_impl(const ssa_plan *plan, const void *x, int B, int H
                                const Variants &var, void *workspace, size_t workspace_bytes, void *stream) {
   if (!plan) return fail(SSA_ERR_NULL, "plan is NULL");
   ssa_status s = check_shape(B, plan->C, H, W, plan->G, plan->h);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if (!x || !out || !workspace) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(x) || !aligned16(out)) return fail(SSA_ERR_ALIGNMENT, "x and out must be 16-byte aligned");
@@ -501,6 +511,7 @@ ssa_status ssa_gn_stats(const void *x, int B, int C, int N, int num_groups, ssa_
                         float *gn_shift, void *stream) {
   if (num_groups <= 0) return fail(SSA_ERR_CONSTRAINT, "num_groups must be positive");
   ssa_status s = check_shape(B, C, N, 1, num_groups, 0);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   if (!x || !norm_weight || !norm_bias || !gn_scale || !gn_shift) return fail(SSA_ERR_NULL, "a required pointer is NULL");
@@ -518,6 +529,7 @@ ssa_status ssa_pack_weights(int C, int num_heads, ssa_dtype dtype, const void *q
                             uint16_t *w_o, float *b_o, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(1, C, 1, 1, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   const void *ptrs[] = {q_weight, k_weight, v_weight, out_weight, w_qkv, b_qkv, w_o, b_o};  // biases may be NULL
@@ -534,6 +546,7 @@ ssa_status ssa_qkv_project(const void *x, int B, int C, int H, int W, int num_he
                            uint16_t *q, uint16_t *k, uint16_t *vt, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   if (!x || !gn_scale || !gn_shift || !w_qkv || !b_qkv || !q || !k || !vt)
@@ -558,6 +571,7 @@ ssa_status ssa_qkv_project_rope(const void *x, int B, int C, int H, int W, int n
                                 const float *b_qkv, uint16_t *q, uint16_t *k, uint16_t *vt, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   if (!x || !gn_scale || !gn_shift || !w_qkv || !b_qkv || !q || !k || !vt)
@@ -584,6 +598,7 @@ ssa_status ssa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int num_heads, uint16_t *o, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, N, 1, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
@@ -601,6 +616,7 @@ ssa_status ssa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v
 ssa_status ssa_rope(uint16_t *q, uint16_t *k, int B, int C, int N, int num_heads, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, N, 1, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if (!q || !k) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   const Dims dm = make_dims(B, C, N, 1, 1, num_heads);
@@ -614,6 +630,7 @@ ssa_status ssa_qk_norm(uint16_t *q, uint16_t *k, int B, int C, int N, int num_he
                        const void *q_norm_weight, const void *k_norm_weight, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, N, 1, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   if (!q || !k || !q_norm_weight || !k_norm_weight) return fail(SSA_ERR_NULL, "a required pointer is NULL");
@@ -641,6 +658,7 @@ ssa_status ssa_attention_ex(const uint16_t *q, const uint16_t *k, const uint16_t
                             int num_heads, int causal, const float *rel_packed, uint16_t *o, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
@@ -661,6 +679,7 @@ ssa_status ssa_attention_ws(const uint16_t *q, const uint16_t *k, const uint16_t
                             size_t workspace_bytes, void *stream) {
   if (num_heads <= 0) return fail(SSA_ERR_CONSTRAINT, "num_heads must be positive");
   ssa_status s = check_shape(B, C, H, W, 0, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if (!q || !k || !vt || !o) return fail(SSA_ERR_NULL, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
@@ -685,6 +704,7 @@ ssa_status ssa_attention_ws(const uint16_t *q, const uint16_t *k, const uint16_t
 ssa_status ssa_out_project(const uint16_t *o, const uint16_t *w_o, const float *b_o, const void *x, int B, int C,
                            int H, int W, ssa_dtype dtype, void *out, void *stream) {
   ssa_status s = check_shape(B, C, H, W, 0, 0);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   if (!o || !w_o || !b_o || !x || !out) return fail(SSA_ERR_NULL, "a required pointer is NULL");
@@ -775,6 +795,7 @@ extern "C" ssa_status ssa_forward_static(const void *x, int B, int C, int H, int
                                          const void *out_weight, const void *out_bias, void *out,
                                          ssa_dtype dtype, void *stream) {
   ssa_status s = check_shape(B, C, H, W, num_groups, num_heads);
+  if (s == kEmpty) return SSA_OK;
   if (s != SSA_OK) return s;
   if ((s = check_dtype(dtype)) != SSA_OK) return s;
   // Biases may be NULL (that projection has no bias), as for ssa_forward.

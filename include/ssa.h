@@ -46,7 +46,7 @@ typedef enum {
 
 typedef enum {
     SSA_OK = 0,
-    SSA_ERR_CONSTRAINT = 1,  /* C % num_groups, C % num_heads, or a size <= 0
+    SSA_ERR_CONSTRAINT = 1,  /* C % num_groups, C % num_heads, C <= 0 or a size < 0
                                 (E_CONSTRAINT in the HNDL attention operator doc) */
     SSA_ERR_DTYPE = 2,       /* dtype is not SSA_F32 / SSA_BF16 */
     SSA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
@@ -58,6 +58,11 @@ typedef enum {
 } ssa_status;
 
 typedef struct ssa_plan ssa_plan;
+
+/* Empty problems: with B, H or W zero (C and its split into groups and heads
+ * still valid) every entry point taking the problem shape does no work and
+ * returns SSA_OK at once, without reading its pointers (which may be NULL);
+ * the workspace sizes are 0. */
 
 /* ---------------------------------------------------------------- block --- */
 

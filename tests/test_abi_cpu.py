@@ -91,6 +91,12 @@ def test_bad_shapes_rejected_without_device(lib):
     assert st == 3          # workspace not 256-byte aligned
     st = lib.ssa_forward(fake, 1, 64, 8, 8, 8, 2, *ptrs, fake, 0, fake, 16, None)
     assert st == 5          # workspace too small
+    # empty problems: no work, SSA_OK, NULL pointers not read; bad splits still fail
+    assert lib.ssa_forward(None, 0, 64, 8, 8, 8, 2, *nul, None, 0, None, 0, None) == 0
+    assert lib.ssa_forward(None, 2, 64, 0, 8, 8, 2, *nul, None, 0, None, 0, None) == 0
+    assert lib.ssa_forward(None, 0, 64, 8, 8, 7, 2, *nul, None, 0, None, 0, None) == 1
+    assert lib.ssa_forward(None, -1, 64, 8, 8, 8, 2, *nul, None, 0, None, 0, None) == 1
+    assert ssa.ssa_workspace_size(0, 64, 8, 8, 8, 2) == 0
     # a relative-position table of (2H-1)(2W-1) > 2^31 - 1 entries per head
     st = lib.ssa_pack_rel_table(fake, 0, 30000, 30000, 1, fake, None)
     assert st == 4 and b"relative-position table" in lib.ssa_last_error_string()

@@ -135,6 +135,25 @@ def test_block_past_2_31_elements(ssa):
         torch.cuda.empty_cache()
 
 
+def test_empty_problems(ssa):
+    """B, H or W zero: no work and no error, through the one-shot, planned and
+    step entry points; the output is the empty tensor of x's shape."""
+    wl = wls.WORKLOADS["tiny"]
+    _, p, _ = wls.make_inputs(wl)
+    pd = {k: v.cuda() for k, v in p.items()}
+    plan = ssa.SsaPlan(pd, wl.num_groups, wl.num_heads)
+    try:
+        for shape in ((0, 64, 8, 8), (2, 64, 0, 8), (2, 64, 8, 0)):
+            xd = torch.empty(shape, device="cuda")
+            out = ssa.ssa_forward(xd, pd, wl.num_groups, wl.num_heads)
+            assert out.shape == xd.shape
+            out = plan.forward(xd, causal=True, rope=True)
+            assert out.shape == xd.shape
+            assert ssa.ssa_get_device_status() == 0
+    finally:
+        plan.close()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_in_place(ssa, dt):
     wl = wls.custom("inplace", 2, 128, 8, 16, 8, 2, dt, seed=5)
