@@ -54,6 +54,12 @@ constexpr int STHREADS = 320;  // single mode with variants: producer, MMA, eigh
 constexpr int MAX_SMEM_FALLBACK = 232448;
 constexpr int SM_SMEM_PER_TWO = 115712;  // per-CTA budget when two CTAs share an SM
 constexpr float RESCALE_LOG2 = 8.0f;
+// The pair kernel (head dim 512) takes its exponentials in fp32 and rounds P
+// once to fp16, whose relative precision does not depend on the magnitude:
+// there P may grow to 2^15 (< 65504) before O is rescaled.  Each rescale
+// stalls its output CTA's P V issue while four warps rewrite all 512 columns
+// of O, so the higher bound keeps them to the first few key tiles of a row.
+constexpr float RESCALE_LOG2_PAIR = 15.0f;
 
 struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
@@ -1554,7 +1560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(xi & 1), ab)) { ok = false; break; }
           mx = fmaxf(mx, xch[((xi & 1) * 2 + (half ^ 1)) * 128 + row]);
           const float m_new = fmaxf(m_used, mx * sc);
-          const bool need = (j > sg.j0) && (m_new > m_used + RESCALE_LOG2);
+          const bool need = (j > sg.j0) && (m_new > m_used + RESCALE_LOG2_PAIR);
           const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
           float alpha = 1.f;
           if (j == sg.j0) {
