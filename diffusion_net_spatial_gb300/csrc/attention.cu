@@ -53,13 +53,17 @@ constexpr int THREADS = 192;   // double mode: producer, MMA, four softmax warps
 constexpr int STHREADS = 320;  // single mode with variants: producer, MMA, eight softmax warps
 constexpr int MAX_SMEM_FALLBACK = 232448;
 constexpr int SM_SMEM_PER_TWO = 115712;  // per-CTA budget when two CTAs share an SM
+// Lazy-rescale bounds (log2 of the largest P before O is rescaled).  Where
+// the exponents are rounded to fp16 before the exponential (the fp16-pair
+// paths of the padded head dims), 2^8 keeps them within 2^-9 absolute.  Where
+// the exponentials are taken in fp32 and P is rounded once to fp16, whose
+// relative precision does not depend on the magnitude, P may grow to 2^15
+// (< 65504): a rescale rewrites all of O's columns before the next P V (512
+// of them in the pair kernel, stalling its output CTA), so the higher bound
+// keeps rescales to the first few key tiles of a row (vae16384 block 519.7 ->
+// 446.5 us).
 constexpr float RESCALE_LOG2 = 8.0f;
-// The pair kernel (head dim 512) takes its exponentials in fp32 and rounds P
-// once to fp16, whose relative precision does not depend on the magnitude:
-// there P may grow to 2^15 (< 65504) before O is rescaled.  Each rescale
-// stalls its output CTA's P V issue while four warps rewrite all 512 columns
-// of O, so the higher bound keeps them to the first few key tiles of a row.
-constexpr float RESCALE_LOG2_PAIR = 15.0f;
+constexpr float RESCALE_LOG2_F32 = 15.0f;
 
 struct AttnArgs {
   int N, h, d, dp, ldc, d_o, n_oc, nqb, kpb, nvr, vrows, slot, nst, ntiles, single, tmem_cols, o_col;
@@ -519,12 +523,13 @@ __global__ void __launch_bounds__((SINGLE && VAR != 0) ? STHREADS : THREADS, SIN
       }
       const float m_new = fmaxf(m_used, mx * sc);
       // Lazy rescale: a row raises its reference maximum only when the new
-      // maximum exceeds it by more than 2^RESCALE_LOG2.  The decision is made
+      // maximum exceeds it by more than the bound (RESCALE_LOG2 on the
+      // fp16-pair exponent path, RESCALE_LOG2_F32 otherwise).  The decision is made
       // per warp (any row that needs it), because the tensor-memory accesses
       // that rescale O are warp-collective; rows that did not need it use
       // their own (possibly unit) factor.  Both halves of a row see the same
       // maxima, so they decide alike.
-      const bool need = (j > 0) && (m_new > m_used + RESCALE_LOG2);
+      const bool need = (j > 0) && (m_new > m_used + (args.ones ? RESCALE_LOG2 : RESCALE_LOG2_F32));
       const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
       float alpha = 1.f;
       if (j == 0) {
@@ -1560,7 +1565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           if (!mbar_wait_warp(&bars[PB_XBAR + q4], (uint32_t)(xi & 1), ab)) { ok = false; break; }
           mx = fmaxf(mx, xch[((xi & 1) * 2 + (half ^ 1)) * 128 + row]);
           const float m_new = fmaxf(m_used, mx * sc);
-          const bool need = (j > sg.j0) && (m_new > m_used + RESCALE_LOG2_PAIR);
+          const bool need = (j > sg.j0) && (m_new > m_used + RESCALE_LOG2_F32);
           const bool rescale = __any_sync(0xFFFFFFFFu, need) != 0;
           float alpha = 1.f;
           if (j == sg.j0) {
