@@ -1793,30 +1793,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
           // Part of a tile cut between clusters: publish this part, count in.
           // Layout of a part: [16 column blocks][8 pieces][128 rows][4 floats],
           // so each store (and each load of the merge) moves 512 contiguous
-          // bytes per warp.
-          const int mine = 2 * cid + (sp.ubeg(cid) < sg.cum ? 1 : 0);
-          float *part = args.part + (long long)mine * PART_FLOATS;
-          for (int blk = half * 8; blk < half * 8 + 8; ++blk) {
-            uint32_t t[32];
-            tmem_ld32(lane_base + (uint32_t)(blk * 32), t);
-            tmem_wait_ld();
-#pragma unroll
-            for (int pc = 0; pc < 8; ++pc)
-              __stcg(reinterpret_cast<uint4 *>(part + ((blk * 8 + pc) * 128 + row) * 4),
-                     make_uint4(t[4 * pc], t[4 * pc + 1], t[4 * pc + 2], t[4 * pc + 3]));
-          }
-          if (half == 0) {
-            __stcg(part + PART_O_FLOATS + row, m_row);
-            __stcg(part + PART_O_FLOATS + 128 + row, l_row);
-          }
-          __threadfence();
-          named_bar_sync(1, 256);
+          // bytes per warp.  When every other contributor has already counted
+          // in (typically: this cluster ends its range with the tile's last
+          // piece, the next began its range with the first), this one merges
+          // straight from tensor memory without publishing its own part.
           const int c_lo = sp.owner(sg.cum), c_hi = sp.owner(sg.cum + sg.n - 1);
-          if (warp == 2 && lane == 0) {
-            const uint32_t prev = atomicAdd(args.cnt + sg.t, 1u);
-            *last_flag = prev == (uint32_t)(c_hi - c_lo) ? 1u : 0u;
-          }
+          if (warp == 2 && lane == 0)
+            *last_flag = *reinterpret_cast<volatile uint32_t *>(args.cnt + sg.t) == (uint32_t)(c_hi - c_lo) ? 2u : 0u;
           named_bar_sync(1, 256);
+          if (*last_flag != 2u) {
+            const int mine = 2 * cid + (sp.ubeg(cid) < sg.cum ? 1 : 0);
+            float *part = args.part + (long long)mine * PART_FLOATS;
+            for (int blk = half * 8; blk < half * 8 + 8; ++blk) {
+              uint32_t t[32];
+              tmem_ld32(lane_base + (uint32_t)(blk * 32), t);
+              tmem_wait_ld();
+#pragma unroll
+              for (int pc = 0; pc < 8; ++pc)
+                __stcg(reinterpret_cast<uint4 *>(part + ((blk * 8 + pc) * 128 + row) * 4),
+                       make_uint4(t[4 * pc], t[4 * pc + 1], t[4 * pc + 2], t[4 * pc + 3]));
+            }
+            if (half == 0) {
+              __stcg(part + PART_O_FLOATS + row, m_row);
+              __stcg(part + PART_O_FLOATS + 128 + row, l_row);
+            }
+            __threadfence();
+            named_bar_sync(1, 256);
+            if (warp == 2 && lane == 0) {
+              const uint32_t prev = atomicAdd(args.cnt + sg.t, 1u);
+              *last_flag = prev == (uint32_t)(c_hi - c_lo) ? 1u : 0u;
+            }
+            named_bar_sync(1, 256);
+          }
           if (*last_flag) {
             // Every other part is published: merge them into this one, each
             // rescaled to the common row maximum.
